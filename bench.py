@@ -26,7 +26,9 @@ FLOPs are the causal ones: 4 D H per visible (query, key) pair, i.e.
 """
 
 import argparse
+import contextlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -173,6 +175,98 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------- host buffers and the link
+def gpu_numa_node(local):
+    """NUMA node of the GPU's PCI function as the kernel reports it, or None."""
+    bus = None
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(local)
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(local), "--query-gpu=pci.bus_id",
+                                  "--format=csv,noheader"], capture_output=True, text=True,
+                                 timeout=30).stdout.strip()
+            dom, rest = out.split(":", 1)
+            bus = f"{int(dom, 16):04x}:{rest.lower()}"
+        except Exception:
+            return None
+    try:
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            node = int(f.read().strip())
+    except Exception:
+        return None
+    return node if node >= 0 else None
+
+
+def _node_cpus(node):
+    cpus = set()
+    try:
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            for part in f.read().strip().split(","):
+                if "-" in part:
+                    a, b = part.split("-")
+                    cpus.update(range(int(a), int(b) + 1))
+                elif part:
+                    cpus.add(int(part))
+    except Exception:
+        pass
+    return cpus
+
+
+@contextlib.contextmanager
+def near_gpu(local):
+    """Narrow this process's CPU affinity to the GPU's NUMA node while
+    page-locked host buffers are allocated (pages are placed on the node of
+    the CPU that first touches them), then restore it.  Yields the node, or
+    None when the platform does not say or no allowed CPU is on it."""
+    node = gpu_numa_node(local)
+    old = os.sched_getaffinity(0)
+    cpus = (_node_cpus(node) & old) if node is not None else set()
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        yield node if cpus else None
+    finally:
+        if cpus:
+            os.sched_setaffinity(0, old)
+
+
+def link_gbs(dev_t, host_t, stream, reps=3):
+    """Host-to-device and device-to-host GB/s of plain copies between a
+    page-locked host tensor and a device tensor of the same size, timed
+    with CUDA events on ``stream``."""
+    import torch
+    nbytes = dev_t.numel() * dev_t.element_size()
+    res = []
+    for h2d in (True, False):
+        dst, src = (dev_t, host_t) if h2d else (host_t, dev_t)
+        dst.copy_(src, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        res.append(round(reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9, 1))
+    return res[0], res[1], nbytes
+
+
+def timed_steps(step, K, min_timed_s, stream):
+    """Steps to time: at least K, and enough to fill ``min_timed_s`` seconds
+    so that the 200 ms clock sampler sees the timed region (short workloads
+    run in milliseconds).  One extra untimed step measures the step time."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    step()
+    e1.record(stream)
+    e1.synchronize()
+    ms = max(e0.elapsed_time(e1), 1e-3)
+    return max(K, int(math.ceil(min_timed_s * 1e3 / ms)))
+
+
 # --------------------------------------------------------------- CPU oracle
 def host_inputs(wl, seed=0, device_tensors=None):
     """float32 host copies of the workload's bf16 q, k, v (exact widening)."""
@@ -185,11 +279,17 @@ def host_inputs(wl, seed=0, device_tensors=None):
     return [t.float().cpu().numpy() for t in device_tensors]
 
 
-def cpu_oracle_sample(wl, qkv, budget_s=15.0, seed=0):
-    """Time the fp64 oracle on a bounded sample of the workload: seeded query
-    rows (all heads) against every key they see, growing the row count until
-    the time budget is spent.  Returns (TFLOP/s over the causal pairs
-    evaluated, description, host cores, seconds)."""
+ORACLE_ROWS_PER_CALL = 64
+
+
+def cpu_oracle_sample(wl, qkv, budget_s=15.0, seed=0, max_calls=None):
+    """Time the fp64 oracle on a bounded sample of the workload: calls of
+    ORACLE_ROWS_PER_CALL seeded query rows (all heads) against every key they
+    see, repeated until the time budget is spent (or ``max_calls`` calls).
+    Every call has the same size, so the cpu_baseline leg (several calls)
+    and each step of the reference arm (one call) time the same unit of work.
+    Returns (TFLOP/s over the causal pairs evaluated, description, host
+    cores, seconds, calls)."""
     import numpy as np
 
     import oracle
@@ -198,19 +298,20 @@ def cpu_oracle_sample(wl, qkv, budget_s=15.0, seed=0):
     S, H, D = wl["S"], wl["H"], wl["D"]
     qf, kf, vf = qkv
     cores = len(os.sched_getaffinity(0))
-    n = 4
-    spent, flops, rows_done = 0.0, 0.0, 0
-    while spent < budget_s and rows_done < S:
-        rows = sample_rows(S, n, seed=seed * 7919 + rows_done + 1)
+    n = min(ORACLE_ROWS_PER_CALL, S)
+    spent, flops, rows_done, calls = 0.0, 0.0, 0, 0
+    while spent < budget_s and (max_calls is None or calls < max_calls):
+        rows = sample_rows(S, n, seed=seed * 7919 + calls + 1)
         t0 = time.perf_counter()
         oracle.attention_monolithic(qf, kf, vf, rows=rows)
         spent += time.perf_counter() - t0
         flops += float(np.sum(4.0 * D * H * (rows + 1)))
         rows_done += len(rows)
-        n = min(4 * n, 256)
-    desc = (f"{rows_done} seeded query rows x {H} heads of the {S}-token sequence against "
-            f"every key they see (fp64 NumPy oracle, BLAS threads = host cores)")
-    return flops / spent / 1e12, desc, cores, spent
+        calls += 1
+    desc = (f"{calls} call(s) of {n} seeded query rows x {H} heads of the {S}-token sequence "
+            f"against every key they see ({rows_done} rows; fp64 NumPy oracle, BLAS threads = "
+            f"host cores)")
+    return flops / spent / 1e12, desc, cores, spent, calls
 
 
 # --------------------------------------------------------------- GPU path
@@ -253,11 +354,13 @@ def run_gpu(args, wl, rank, world, local):
     from context_causal_attention_attn_gb300 import build as cpbuild
     from context_causal_attention_attn_gb300.inputs import make_qkv
 
-    if rank == 0 or not os.path.exists(cpbuild.LIB):
-        cpbuild.build()
-    barrier(world)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    # one rank compiles (if needed); the others load the result after the barrier
+    if rank == 0:
+        cpbuild.build()
+    barrier(world)
+    cp.lib()
     S, H, Hkv, D, P, layout = wl["S"], wl["H"], wl["Hkv"], wl["D"], wl["P"], wl["layout"]
     q, k, v = make_qkv(S, H, D, Hkv=Hkv, dtype=torch.bfloat16, seed=rank, device=dev)
     out = torch.empty(S, H, D, dtype=torch.bfloat16, device=dev)
@@ -314,7 +417,8 @@ def run_gpu(args, wl, rank, world, local):
 
     # timed region: per-launch events for the ring (one attention kernel per
     # ring step); whole-step events bracket everything
-    K = args.steps
+    K = timed_steps(step, args.steps, args.min_timed_s, stream)
+    K = int(reduce_max(float(K), world))
     ev_start = torch.cuda.Event(enable_timing=True)
     ev_end = torch.cuda.Event(enable_timing=True)
     per_launch = []
@@ -354,10 +458,16 @@ def run_gpu(args, wl, rank, world, local):
     t_max_ms = reduce_max(total_ms, world)
     clocks = clk.summary()
 
-    # end to end through the public API with pinned host buffers
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    hout = torch.empty(S, H, D, dtype=torch.bfloat16).pin_memory()
-    hlse = torch.empty(H, S, dtype=torch.float32).pin_memory()
+    # end to end through the public API with pinned host buffers on the
+    # GPU's NUMA node
+    with near_gpu(local) as numa_node:
+        hq, hk, hv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v))
+        hout = torch.empty(S, H, D, dtype=torch.bfloat16, pin_memory=True)
+        hlse = torch.empty(H, S, dtype=torch.float32, pin_memory=True)
+    for h_, d_ in ((hq, q), (hk, k), (hv, v)):
+        h_.copy_(d_)
+    h2d_gbs, d2h_gbs, link_bytes = link_gbs(q, hq, stream)
+    q.copy_(hq)
     K_e2e = max(1, min(K, 3))
     host_api = wl["kind"] in ("ring", "ulysses", "usp")
     host_fn = {"ulysses": "cp_ulysses_forward_host", "usp": "cp_usp_forward_host"}.get(
@@ -434,6 +544,7 @@ def run_gpu(args, wl, rank, world, local):
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
+        "steps_requested": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(t_max_ms / K, 3),
         "higher_is_better": True,
@@ -455,7 +566,13 @@ def run_gpu(args, wl, rank, world, local):
                 "steps": K_e2e,
                 "api": (host_fn + f" (pinned host buffers, {groups} head groups, copies on a "
                         "second stream)") if host_api else
-                       "pinned host copies + device entry point on one stream"},
+                       "pinned host copies + device entry point on one stream",
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                "link_note": (f"plain pinned copies of q ({link_bytes >> 20} MiB) each way; "
+                              f"host buffers on NUMA node {numa_node}" if numa_node is not None
+                              else f"plain pinned copies of q ({link_bytes >> 20} MiB) each "
+                              "way; the GPU's NUMA node is not reported, host buffers where "
+                              "the allocator put them")},
     }
     peaks, peak_kind = load_peaks()
     if wl["kind"] in ("ring", "ring_copy"):
@@ -489,20 +606,21 @@ def run_gpu(args, wl, rank, world, local):
         result["per_virtual_rank_ms"] = per
         result["virtual_rank_imbalance"] = imb
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        val, desc, cores, spent = cpu_oracle_sample(wl, host_inputs(wl, device_tensors=(q, k, v)),
-                                                    budget_s=args.cpu_budget)
+        val, desc, cores, spent, _ = cpu_oracle_sample(
+            wl, host_inputs(wl, device_tensors=(q, k, v)), budget_s=args.cpu_budget)
         result["cpu_baseline"] = {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores,
                                   "kind": "oracle", "sample": desc,
                                   "seconds": round(spent, 1)}
     return result
 
 
-def cpu_oracle_bwd_sample(wl, budget_s=15.0, seed=0, with_forward=False):
-    """Time the fp64 oracle backward on a bounded sample: seeded query rows of
-    one head against every key they see (out and lse of those rows from the
-    oracle's forward, timed only when with_forward).  Returns (TFLOP/s counted
-    as 2.5x -- 3.5x with the forward -- the causal forward FLOPs of the pairs
-    evaluated, description, cores, seconds)."""
+def cpu_oracle_bwd_sample(wl, budget_s=15.0, seed=0, with_forward=False, max_calls=None):
+    """Time the fp64 oracle backward on a bounded sample: calls of
+    ORACLE_ROWS_PER_CALL seeded query rows of one head against every key they
+    see (out and lse of those rows from the oracle's forward, timed only when
+    with_forward), until the budget is spent or ``max_calls`` calls.  Returns
+    (TFLOP/s counted as 2.5x -- 3.5x with the forward -- the causal forward
+    FLOPs of the pairs evaluated, description, cores, seconds, calls)."""
     import numpy as np
     import torch
 
@@ -514,9 +632,9 @@ def cpu_oracle_bwd_sample(wl, budget_s=15.0, seed=0, with_forward=False):
     do = make_dout(S, 1, D, dtype=torch.bfloat16, seed=seed)
     qf, kf, vf, dof = (t.double().numpy() for t in (q, k, v, do))
     cores = len(os.sched_getaffinity(0))
-    n, spent, flops, rows_done = 4, 0.0, 0.0, 0
-    while spent < budget_s and rows_done < S:
-        rows = sample_rows(S, n, seed=seed * 7919 + rows_done + 1)
+    n, spent, flops, rows_done, calls = min(ORACLE_ROWS_PER_CALL, S), 0.0, 0.0, 0, 0
+    while spent < budget_s and (max_calls is None or calls < max_calls):
+        rows = sample_rows(S, n, seed=seed * 7919 + calls + 1)
         kmax = int(rows.max()) + 1
         t0 = time.perf_counter()
         o, l = oracle.attention(qf[rows], kf[:kmax], vf[:kmax], q_positions=rows)
@@ -526,11 +644,11 @@ def cpu_oracle_bwd_sample(wl, budget_s=15.0, seed=0, with_forward=False):
         spent += time.perf_counter() - (t0 if with_forward else t1)
         flops += (3.5 if with_forward else 2.5) * float(np.sum(4.0 * D * (rows + 1)))
         rows_done += len(rows)
-        n = min(4 * n, 256)
-    desc = (f"{'forward + ' if with_forward else ''}backward of {rows_done} seeded query rows "
-            f"of one head of the {S}-token sequence against every key they see (fp64 NumPy "
-            f"oracle, BLAS threads = host cores)")
-    return flops / spent / 1e12, desc, cores, spent
+        calls += 1
+    desc = (f"{'forward + ' if with_forward else ''}backward of {calls} call(s) of {n} seeded "
+            f"query rows of one head of the {S}-token sequence against every key they see "
+            f"({rows_done} rows; fp64 NumPy oracle, BLAS threads = host cores)")
+    return flops / spent / 1e12, desc, cores, spent, calls
 
 
 def run_bwd(args, wl, rank, world, local):
@@ -543,11 +661,13 @@ def run_bwd(args, wl, rank, world, local):
     from context_causal_attention_attn_gb300 import build as cpbuild
     from context_causal_attention_attn_gb300.inputs import make_dout, make_qkv
 
-    if rank == 0 or not os.path.exists(cpbuild.LIB):
-        cpbuild.build()
-    barrier(world)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    # one rank compiles (if needed); the others load the result after the barrier
+    if rank == 0:
+        cpbuild.build()
+    barrier(world)
+    cp.lib()
     S, H, Hkv, D, P, layout = wl["S"], wl["H"], wl["Hkv"], wl["D"], wl["P"], wl["layout"]
     train = wl["kind"] == "ring_train"
     q, k, v = make_qkv(S, H, D, Hkv=Hkv, dtype=torch.bfloat16, seed=rank, device=dev)
@@ -584,7 +704,8 @@ def run_bwd(args, wl, rank, world, local):
     for _ in range(args.warmup):
         step()
     cp.cp_check_device_error(stream)
-    K = args.steps
+    K = timed_steps(step, args.steps, args.min_timed_s, stream)
+    K = int(reduce_max(float(K), world))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
            for _ in range(K)]
     barrier(world)
@@ -606,9 +727,15 @@ def run_bwd(args, wl, rank, world, local):
     t_max_ms = reduce_max(total_ms, world)
     clocks = clk.summary()
 
-    # end to end: inputs from pinned host memory, gradients back
-    host_in = [t.cpu().pin_memory() for t in ((q, k, v, do) if train else (q, k, v, do, out, lse))]
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    # end to end: inputs from pinned host memory (on the GPU's NUMA node),
+    # gradients back
+    src = (q, k, v, do) if train else (q, k, v, do, out, lse)
+    with near_gpu(local) as numa_node:
+        host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in src]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    for h_, d_ in zip(host_in, src):
+        h_.copy_(d_)
+    h2d_gbs, d2h_gbs, link_bytes = link_gbs(dq, host_out[0], stream)
     K_e2e = max(1, min(K, 3))
     host_api = not train
     if host_api:
@@ -670,6 +797,7 @@ def run_bwd(args, wl, rank, world, local):
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
+        "steps_requested": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(t_max_ms / K, 3),
         "higher_is_better": True,
@@ -695,7 +823,12 @@ def run_bwd(args, wl, rank, world, local):
                 "steps": K_e2e,
                 "api": (f"cp_ring_backward_host (pinned host buffers, {groups} head groups, "
                         "copies on a second stream)") if host_api else
-                       "pinned host copies + device entry points on one stream"},
+                       "pinned host copies + device entry points on one stream",
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                "link_note": (f"plain pinned copies of {link_bytes >> 20} MiB each way; host "
+                              f"buffers on NUMA node {numa_node}" if numa_node is not None else
+                              f"plain pinned copies of {link_bytes >> 20} MiB each way; the "
+                              "GPU's NUMA node is not reported")},
         "roofline": {
             "kernel": kernel_names[top], "bound": "tensor", "achieved": round(achieved, 2),
             "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
@@ -705,8 +838,8 @@ def run_bwd(args, wl, rank, world, local):
                      f"({shares[top] / K:.2f} ms per step)")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        val, desc, cores, spent = cpu_oracle_bwd_sample(wl, budget_s=args.cpu_budget,
-                                                        with_forward=train)
+        val, desc, cores, spent, _ = cpu_oracle_bwd_sample(wl, budget_s=args.cpu_budget,
+                                                           with_forward=train)
         result["cpu_baseline"] = {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores,
                                   "kind": "oracle", "sample": desc, "seconds": round(spent, 1)}
     return result
@@ -720,11 +853,13 @@ def run_hbm(args, wl, rank, world, local):
     from context_causal_attention_attn_gb300 import build as cpbuild
     from context_causal_attention_attn_gb300.inputs import make_qkv
 
-    if rank == 0 or not os.path.exists(cpbuild.LIB):
-        cpbuild.build()
-    barrier(world)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    # one rank compiles (if needed); the others load the result after the barrier
+    if rank == 0:
+        cpbuild.build()
+    barrier(world)
+    cp.lib()
     stream = torch.cuda.current_stream(dev)
     S, H, Hkv, D, P = wl["S"], wl["H"], wl["Hkv"], wl["D"], wl["P"]
     g = torch.Generator(device=dev)
@@ -761,7 +896,8 @@ def run_hbm(args, wl, rank, world, local):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    K = args.steps
+    K = timed_steps(step, args.steps, args.min_timed_s, stream)
+    K = int(reduce_max(float(K), world))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -772,9 +908,14 @@ def run_hbm(args, wl, rank, world, local):
         e1.record(stream)
         torch.cuda.synchronize(dev)
     t_ms = reduce_max(e0.elapsed_time(e1), world)
-    # end to end with pinned host buffers
-    hin = [t.cpu().pin_memory() for t in inputs]
-    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in result_t]
+    # end to end with pinned host buffers (on the GPU's NUMA node)
+    with near_gpu(local) as numa_node:
+        hin = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in inputs]
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in result_t]
+    for h_, d_ in zip(hin, inputs):
+        h_.copy_(d_)
+    h2d_gbs, d2h_gbs, _ = link_gbs(inputs[0], hin[0], stream)
+    inputs[0].copy_(hin[0])
     K_e2e = max(1, min(K, 3))
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
@@ -794,6 +935,7 @@ def run_hbm(args, wl, rank, world, local):
     return {
         "metric": f"{kernel} HBM throughput ({args.workload})", "value": round(gbs, 1),
         "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "steps_requested": args.steps,
         "ms_per_step": round(t_ms / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if wl["kind"] == "merge" else "bf16",
         "data": "synthetic (seeded N(0,1), drawn on device)",
@@ -805,7 +947,8 @@ def run_hbm(args, wl, rank, world, local):
         "gpu_launches": K * launches,
         "e2e": {"value": round(world * algo * K_e2e / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in inputs),
-                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in result_t)},
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in result_t),
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "host_numa_node": numa_node},
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs / world, 1),
                      "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                      "frac": round(gbs / world / float(peaks["hbm_gbs"]), 4), "traffic": None,
@@ -817,23 +960,26 @@ def run_reference(args, wl, rank, world):
     """The fp64 oracle as it stands on the host cores, same metric and unit."""
     if rank != 0:
         return None
-    vals = []
+    vals, secs = [], []
     cores = len(os.sched_getaffinity(0))
     desc = ""
-    spent_total = 0.0
-    budget = max(2.0, args.cpu_budget / max(1, args.steps + args.warmup))
     bwd = wl["kind"] in ("ring_bwd", "ring_train")
     qkv = None if bwd else host_inputs(wl)
+    # one step = one oracle call of the same size the cpu_baseline leg times
+    # (ORACLE_ROWS_PER_CALL rows), so both report the same rate
     for i in range(args.warmup + args.steps):
         if bwd:
-            val, desc, cores, spent = cpu_oracle_bwd_sample(
-                wl, budget_s=budget, seed=i, with_forward=wl["kind"] == "ring_train")
+            val, desc, cores, spent, _ = cpu_oracle_bwd_sample(
+                wl, budget_s=math.inf, seed=i, with_forward=wl["kind"] == "ring_train",
+                max_calls=1)
         else:
-            val, desc, cores, spent = cpu_oracle_sample(wl, qkv, budget_s=budget, seed=i)
-        spent_total += spent
+            val, desc, cores, spent, _ = cpu_oracle_sample(wl, qkv, budget_s=math.inf, seed=i,
+                                                           max_calls=1)
         if i >= args.warmup:
             vals.append(val)
-    v = statistics.fmean(vals)
+            secs.append(spent)
+    # rate of all timed steps together: FLOPs / seconds summed over steps
+    v = sum(x * t for x, t in zip(vals, secs)) / sum(secs)
     S = wl["S"]
     return {
         "impl": "reference",
@@ -843,7 +989,7 @@ def run_reference(args, wl, rank, world):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": None,
+        "ms_per_step": round(1e3 * statistics.fmean(secs), 1),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -852,7 +998,8 @@ def run_reference(args, wl, rank, world):
         "config": {"workload": args.workload, "S": S, "H": wl["H"], "Hkv": wl["Hkv"],
                    "D": wl["D"], "P": wl["P"], "layout": wl["layout"]},
         "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores,
-                         "kind": "oracle", "sample": desc + f" (each step ~{budget:.0f} s)"},
+                         "kind": "oracle",
+                         "sample": f"each step: {desc}; {args.steps} timed steps"},
         "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -868,6 +1015,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU oracle time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-timed-s", type=float, default=2.0,
+                    help="time at least this long (more than --steps steps for short "
+                         "workloads) so that the 200 ms clock sampler covers the timed region")
     ap.add_argument("--host-groups", type=int, default=8,
                     help="head groups of the host-buffer ring in the end-to-end measurement")
     args = ap.parse_args()

@@ -2,12 +2,17 @@
 
 Each CUDA source is compiled in parallel to an object in ``_build/`` and the
 objects are linked into ``context_causal_attention_attn_gb300/libcpattn.so``.
-Rebuilds only when a source or header is newer than the library.
+Rebuilds only when a source or header is newer than the library.  Builds
+are serialised across processes by an exclusive lock on ``_build/.lock``, so
+several processes (ranks of one job, test workers) may call build() at once:
+the first compiles, the others wait and find the library up to date.
 
     python -m context_causal_attention_attn_gb300.build [--force]
 """
 
 import concurrent.futures as cf
+import contextlib
+import fcntl
 import glob
 import os
 import shutil
@@ -58,11 +63,28 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
+@contextlib.contextmanager
+def _locked():
+    os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as f:
+        fcntl.flock(f, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(f, fcntl.LOCK_UN)
+
+
 def build(force=False, verbose=False, extra=()):
     """Compile and link; returns the path of the library."""
     if not force and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    with _locked():
+        if not force and up_to_date():
+            return LIB
+        return _build(verbose, extra)
+
+
+def _build(verbose, extra):
     extra = list(extra)
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         results = list(ex.map(lambda s: _compile(s, extra), sources()))

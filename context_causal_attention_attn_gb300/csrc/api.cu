@@ -878,6 +878,9 @@ class HostGroupPipeline {
     }
   }
   ~HostGroupPipeline() {
+    // an early return (a failed launch) still joins the copy streams, so the
+    // caller's host buffers are free once the compute stream has passed
+    finish();
     // both are released once the device has passed them
     for (cudaEvent_t e : ev_)
       if (e) cudaEventDestroy(e);
@@ -905,15 +908,23 @@ class HostGroupPipeline {
     if (overlap_ && check(cudaEventRecord(ev_[G_ + g], cs_)))
       check(cudaStreamWaitEvent(os_, ev_[G_ + g], 0));
   }
-  // the compute stream waits for the last copy in each direction
+  // The compute stream waits for the last copy in each direction.  This
+  // runs after an error too (then from the destructor), so that no copy the
+  // call enqueued outlives the compute stream's later work.
   void finish() {
-    if (!overlap_ || !ok()) return;
-    if (check(cudaEventRecord(ev_[2 * G_], xs_))) check(cudaStreamWaitEvent(cs_, ev_[2 * G_], 0));
-    if (check(cudaEventRecord(ev_[2 * G_ + 1], os_)))
-      check(cudaStreamWaitEvent(cs_, ev_[2 * G_ + 1], 0));
+    if (!overlap_ || joined_) return;
+    joined_ = true;
+    join(xs_, ev_[2 * G_]);
+    join(os_, ev_[2 * G_ + 1]);
   }
 
  private:
+  void join(cudaStream_t from, cudaEvent_t e) {
+    cudaError_t r = e ? cudaEventRecord(e, from) : cudaErrorInvalidResourceHandle;
+    if (r == cudaSuccess) r = cudaStreamWaitEvent(cs_, e, 0);
+    if (r != cudaSuccess) r = cudaStreamSynchronize(from);  // no event: wait on the host
+    check(r);
+  }
   bool check(cudaError_t e) {
     if (err_ == cudaSuccess) err_ = e;
     return err_ == cudaSuccess;
@@ -924,6 +935,7 @@ class HostGroupPipeline {
   bool overlap_;
   std::vector<cudaEvent_t> ev_;
   cudaError_t err_ = cudaSuccess;
+  bool joined_ = false;
 };
 
 // Device staging of cp_ring_forward_host: q, k, v, out, lse of every group

@@ -716,15 +716,15 @@ template <bool kDKDV, bool kStriped>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                                 int ctas, int* dev_err, cudaStream_t stream) {
-  static bool attr_set = false;
   constexpr uint32_t bytes = bw::Smem<kDKDV>::BYTES;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<kDKDV, kStriped>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the shared-memory attribute is a property of the function on each device
+  static PerDeviceOnce attr_once;
+  const cudaError_t e = once_per_device(attr_once, [] {
+    return cudaFuncSetAttribute(attn_bwd_tc_kernel<kDKDV, kStriped>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes));
+  });
+  if (e != cudaSuccess) return e;
   attn_bwd_tc_kernel<kDKDV, kStriped><<<ctas, bw::THREADS, bytes, stream>>>(tq, tk, tv, tdo, p,
                                                                            dev_err);
   return cudaGetLastError();

@@ -101,7 +101,9 @@ __global__ void __launch_bounds__(kSimtRows)
   }
 
   // ---------------------------------------------------------- epilogue
-  const float lse_blk = l > 0.f ? m + logf(l) : -CUDART_INF_F;
+  // l == 0 exactly when no key was visible (a NaN score leaves l NaN, which
+  // then reaches lse and out)
+  const float lse_blk = l != 0.f ? m + logf(l) : -CUDART_INF_F;
   const int64_t orow =
       it.o_row + static_cast<int64_t>(b) * it.b_o_rows + static_cast<int64_t>(row) * it.o_stride;
   const int64_t oel = (orow * p.H + head) * static_cast<int64_t>(D);
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kSimtRows)
   if (merge) {
     const float a = *lse_ptr;
     const float hi = fmaxf(a, lse_blk);
-    if (hi == -CUDART_INF_F) {
+    if (a == -CUDART_INF_F && lse_blk == -CUDART_INF_F) {  // both empty (not NaN)
       w_blk = 0.f;
       lse_new = -CUDART_INF_F;
     } else {
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kSimtRows)
       w_blk = expf(lse_blk - lse_new);
     }
   }
-  const float c_blk = l > 0.f ? w_blk / l : 0.f;
+  const float c_blk = l != 0.f ? w_blk / l : 0.f;
   float* accp = p.acc + oel;
 #pragma unroll
   for (int d = 0; d < D; d += 4) {

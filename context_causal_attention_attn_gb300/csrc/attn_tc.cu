@@ -568,14 +568,15 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
       const float* lse_stg = reinterpret_cast<const float*>(smem + C::OFF_LSE);
       const float LOG2E = 1.4426950408889634f;
       const float LN2 = 0.6931471805599453f;
-      // block result in log2 units
-      const float lse_blk2 = l > 0.f ? m_used + __log2f(l) : -CUDART_INF_F;
+      // block result in log2 units; l == 0 exactly when no key was visible
+      // (a NaN score leaves l NaN, which then reaches lse and out)
+      const float lse_blk2 = l != 0.f ? m_used + __log2f(l) : -CUDART_INF_F;
       const bool final_out = (it.flags & kFlagFinal) != 0;
       float w_acc = 0.f, w_blk = 1.f, lse_new2 = lse_blk2;
       if (merge) {
         const float a2 = valid ? lse_stg[row] * LOG2E : -CUDART_INF_F;
         const float hi = fmaxf(a2, lse_blk2);
-        if (hi == -CUDART_INF_F) {
+        if (a2 == -CUDART_INF_F && lse_blk2 == -CUDART_INF_F) {  // both empty (not NaN)
           w_acc = 0.f;
           w_blk = 0.f;
           lse_new2 = -CUDART_INF_F;
@@ -586,7 +587,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
           w_blk = ex2_approx(lse_blk2 - lse_new2);
         }
       }
-      const float c_blk = l > 0.f ? w_blk / l : 0.f;
+      const float c_blk = l != 0.f ? w_blk / l : 0.f;
       if (ok) {
         float* stg = reinterpret_cast<float*>(smem + C::OFF_Q);
         const int wrow0 = quad * 32;                // this warp's rows
@@ -675,18 +676,19 @@ cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const AttnParams& p, int ctas, int* dev_err, cudaStream_t stream,
                            bool dependent) {
   using C = tc::Cfg<kNT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<false, kNT>,
+  // the shared-memory attribute is a property of the function on each device
+  static PerDeviceOnce attr_once;
+  cudaError_t e = once_per_device(attr_once, [] {
+    cudaError_t r = cudaFuncSetAttribute(attn_fwd_tc_kernel<false, kNT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::SMEM_BYTES));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_fwd_tc_kernel<true, kNT>,
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(attn_fwd_tc_kernel<true, kNT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(C::SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   // dependent: launched with programmatic stream serialisation, so that it
   // overlaps the tail of the previous kernel on the stream (which must be
   // this kernel, writing none of q, k, v)

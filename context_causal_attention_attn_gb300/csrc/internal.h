@@ -6,9 +6,41 @@
 // to two key segments, with global positions for the causal mask.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace cpattn {
+
+// ------------------------------------------------------- per-device set-up
+// Host-side state that belongs to one device (a kernel's shared-memory
+// attribute, a symbol's device address) is set up once per device, with
+// that device current, and is safe to reach from several host threads.
+constexpr int kMaxDevices = 64;
+
+struct PerDeviceOnce {
+  std::atomic<bool> done[kMaxDevices] = {};
+  std::mutex mu;
+};
+
+// Runs fn() on the current device the first time this device reaches `o`;
+// later calls return cudaSuccess without running it.  A failing fn() is
+// retried on the next call.
+template <class F>
+cudaError_t once_per_device(PerDeviceOnce& o, F&& fn) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (o.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(o.mu);
+  if (o.done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess) o.done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 constexpr int kMaxItems = 32;   // 2 items per virtual rank per ring step
 constexpr int kMaxSegs = 2;     // zigzag: a late query chunk sees 2 KV chunks

@@ -17,16 +17,21 @@ __device__ int g_dev_status;
 // Resident blocks per SM used to size the grid-stride kernels below.
 constexpr int kStreamThreads = 256;
 
+// Device address of g_dev_status on the current device (looked up once per
+// device with that device current; the symbol's name is only a host-side
+// stand-in in host code).
 int* device_status_ptr() {
-  static int* ptrs[64] = {nullptr};
+  static PerDeviceOnce once;
+  static int* ptrs[kMaxDevices] = {nullptr};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (ptrs[dev] == nullptr) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const cudaError_t e = once_per_device(once, [dev] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dev_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
-  }
-  return ptrs[dev];
+    const cudaError_t r = cudaGetSymbolAddress(&p, g_dev_status);
+    if (r == cudaSuccess) ptrs[dev] = static_cast<int*>(p);
+    return r;
+  });
+  return e == cudaSuccess ? ptrs[dev] : nullptr;
 }
 
 static int stream_grid(int64_t work_items) {
@@ -59,12 +64,10 @@ __global__ void __launch_bounds__(kStreamThreads)
   const int64_t n_rh = Sq * H;
   const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const float LOG2E = 1.4426950408889634f;
-  const float LN2 = 0.6931471805599453f;
   constexpr int64_t kStep = static_cast<int64_t>(GROUPS_PER_WARP) * U;
   for (int64_t base = warp_id * kStep; base < n_rh; base += warps_total * kStep) {
     for (int v = 0; v < vec_per_lane; ++v) {
-      float a2[U], b2[U];
+      float lsa[U], lsb[U];
       float4 x[U], y[U];
       int64_t off[U];
       bool act[U];
@@ -72,15 +75,15 @@ __global__ void __launch_bounds__(kStreamThreads)
       for (int u = 0; u < U; ++u) {
         const int64_t rh = base + u * GROUPS_PER_WARP + grp;  // head-major: h * Sq + i
         act[u] = rh < n_rh;
-        a2[u] = -CUDART_INF_F;
-        b2[u] = -CUDART_INF_F;
+        lsa[u] = -CUDART_INF_F;
+        lsb[u] = -CUDART_INF_F;
         off[u] = 0;
         if (act[u]) {
           const int64_t h = rh / Sq;
           const int64_t i = rh - h * Sq;
           off[u] = (i * H + h) * static_cast<int64_t>(D) / 4 + v * L + sub;
-          a2[u] = lse_acc[rh];
-          b2[u] = lse_blk[rh];
+          lsa[u] = lse_acc[rh];
+          lsb[u] = lse_blk[rh];
           x[u] = reinterpret_cast<const float4*>(out_acc)[off[u]];
           y[u] = __ldcs(reinterpret_cast<const float4*>(out_blk) + off[u]);
         }
@@ -88,27 +91,30 @@ __global__ void __launch_bounds__(kStreamThreads)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (!act[u]) continue;
-        // weights in the log2 domain
-        const float la = a2[u] * LOG2E, lb = b2[u] * LOG2E;
+        // Natural-log domain with the accurate expf / log1pf: the kernel is
+        // bound by HBM, so the exact-rounding functions cost nothing and
+        // keep fp32 merges within a few ulp of the exact result.  A -inf
+        // side gets weight exp(-inf) = 0; both -inf leave (-inf, 0); a NaN
+        // side makes the result NaN.
+        const float la = lsa[u], lb = lsb[u];
         const float hi = fmaxf(la, lb);
-        float wa = 0.f, wb = 0.f, lse2 = -CUDART_INF_F;
-        if (hi != -CUDART_INF_F) {
-          const float ea = sm100::ex2_approx(la - hi), eb = sm100::ex2_approx(lb - hi);
-          lse2 = hi + __log2f(ea + eb);
-          wa = sm100::ex2_approx(la - lse2);
-          wb = sm100::ex2_approx(lb - lse2);
+        float wa = 0.f, wb = 0.f, lse = -CUDART_INF_F;
+        if (!(la == -CUDART_INF_F && lb == -CUDART_INF_F)) {
+          lse = hi + log1pf(expf(-fabsf(la - lb)));
+          wa = expf(la - lse);
+          wb = expf(lb - lse);
         }
         reinterpret_cast<float4*>(out_acc)[off[u]] =
             make_float4(fmaf(x[u].x, wa, y[u].x * wb), fmaf(x[u].y, wa, y[u].y * wb),
                         fmaf(x[u].z, wa, y[u].z * wb), fmaf(x[u].w, wa, y[u].w * wb));
-        a2[u] = lse2 == -CUDART_INF_F ? -CUDART_INF_F : lse2 * LN2;
+        lsa[u] = lse;
       }
       // every lane of a group has read the old lse before one writes the new
       __syncwarp();
       if (v == vec_per_lane - 1 && sub == 0) {
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (act[u]) lse_acc[base + u * GROUPS_PER_WARP + grp] = a2[u];
+          if (act[u]) lse_acc[base + u * GROUPS_PER_WARP + grp] = lsa[u];
       }
       __syncwarp();
     }

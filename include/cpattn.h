@@ -242,6 +242,11 @@ int cp_ring_forward_copy(const void* q, const void* k, const void* v, cp_dtype i
  *   cp_ring_forward apply to each group.  The call creates (and releases)
  *   events and a stream, so it is meant for direct calls, not for capture
  *   into a CUDA graph; the same holds for every *_host entry point below.
+ *   Errors: a failure after copies were enqueued (a failed launch) still
+ *   makes `stream` wait for every copy the call enqueued before it returns
+ *   the error, so after synchronising `stream` no copy touches the host
+ *   buffers or the workspace; their contents are then unspecified.  The
+ *   same holds for every *_host entry point below.
  */
 int64_t cp_ring_host_workspace_size(int64_t S, int H, int Hkv, int D, int groups,
                                     cp_dtype in_dt, cp_dtype out_dt);

@@ -11,7 +11,7 @@ Definition followed ([CP-handbook], section "哪些运算可以直接切", the
     lse[h, i]       = log sum_j exp(scores[h, i, j])                  [H, Sq]
     out[i, h, :]    = sum_j exp(scores[h, i, j] - lse[h, i]) v[j, h, :]
 
-Readings where the page is silent (each also listed in the design doc):
+Readings where the page is silent:
 
 * GQA: the page's helper needs equal head counts.  Query head h reads KV head
   h // (H // Hkv) (contiguous groups of H/Hkv query heads share a KV head).

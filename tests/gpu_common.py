@@ -41,3 +41,28 @@ def compare(out, lse, ref_out, ref_lse, atol_out, atol_lse, rows=None):
             f"{ref_out[idx]:.6f}; max|dlse|={d_lse:.3e} (tol {atol_lse}); rows with "
             f"|dout|>tol: {np.unique(np.argwhere(err > atol_out)[:, 0])[:10]}")
     return d_out, d_lse
+
+
+# Guard bands: results written through a view into a larger buffer whose
+# head and tail hold a sentinel; a kernel that writes past either end of its
+# output (a ragged tail, a striped row stride, a host copy's pitch) changes
+# a sentinel, which value comparisons inside the tensor would not see.
+SENTINEL = -12288.0  # exact in bf16 and fp32, far outside any result
+
+
+def guarded(shape, dtype, device="cuda", guard_rows=2, pin=False):
+    """A tensor of ``shape`` inside a sentinel-filled buffer with at least
+    ``guard_rows`` rows (of the last dimensions) before and after it, both
+    bands a multiple of 64 elements (16-byte aligned views).  Returns (view,
+    intact) where intact() tells whether both bands still hold the
+    sentinel."""
+    n = int(np.prod(shape))
+    row = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    g = -(-max(guard_rows * row, 64) // 64) * 64
+    kw = {"pin_memory": True} if pin else {"device": device}
+    buf = torch.full((n + 2 * g,), SENTINEL, dtype=dtype, **kw)
+    view = buf[g:g + n].view(shape)
+
+    def intact():
+        return bool((buf[:g] == SENTINEL).all()) and bool((buf[g + n:] == SENTINEL).all())
+    return view, intact

@@ -23,7 +23,7 @@ import torch
 
 import oracle
 from context_causal_attention_attn_gb300.inputs import make_dout, make_qkv, sample_rows
-from gpu_common import host
+from gpu_common import guarded, host
 
 pytestmark = pytest.mark.gpu
 
@@ -224,13 +224,14 @@ def test_ring_backward_ragged(cp, layout, S, P):
     """Chunk counts that do not divide S (short / empty last chunks, partial
     tiles inside chunks) and a striped case with 200-row stripes."""
     q, k, v, do, ob, l32 = forward_inputs(S, 2, 1, seed=S + P)
-    dq, dk, dv = cp.cp_ring_backward(*dev(q, k, v, ob, do, l32), P, layout,
-                                     grad_dtype=torch.float32)
+    (dq, dq_ok), (dk, dk_ok), (dv, dv_ok) = (guarded(t.shape, torch.float32) for t in (q, k, v))
+    cp.cp_ring_backward(*dev(q, k, v, ob, do, l32), P, layout, dq=dq, dk=dk, dv=dv)
     cp.cp_check_device_error()
     rq, rk, rv = oracle_grads(q, k, v, do, ob, l32)
     grads_close(dq, rq, "dq")
     grads_close(dk, rk, "dk")
     grads_close(dv, rv, "dv")
+    assert dq_ok() and dk_ok() and dv_ok(), "write outside dq / dk / dv"
 
 
 def test_ring_backward_matches_block_sum(cp):
@@ -343,12 +344,15 @@ def test_ring_backward_host_equals_device(cp, layout, H, Hkv, groups, grad_dtype
                               grad_dtype=grad_dtype)
     host = [t.pin_memory() for t in (q, k, v, out.cpu(), do, lse.cpu())]
     side = torch.cuda.Stream() if two_streams else None
-    got = cp.cp_ring_backward_host(*host, P, layout, grad_dtype=grad_dtype, groups=groups,
+    (hdq, dq_ok), (hdk, dk_ok), (hdv, dv_ok) = (guarded(t.shape, grad_dtype, pin=True)
+                                                for t in (q, k, v))
+    got = cp.cp_ring_backward_host(*host, P, layout, hdq=hdq, hdk=hdk, hdv=hdv, groups=groups,
                                    copy_stream=side)
     torch.cuda.current_stream().synchronize()
     cp.cp_check_device_error()
     for g, r in zip(got, ref):
         assert torch.equal(g, r.cpu())
+    assert dq_ok() and dk_ok() and dv_ok(), "write outside the host dq / dk / dv"
 
 
 def test_ring_backward_host_fp32_toy(cp):

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from context_causal_attention_attn_gb300.inputs import make_qkv
-from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, host
+from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, guarded, host
 
 pytestmark = pytest.mark.gpu
 
@@ -42,12 +42,15 @@ F32_CASES = [  # Sq, Sk, H, Hkv, D, causal, q_off, k_off
 def test_block_fp32(cp, case):
     Sq, Sk, H, Hkv, D, causal, qo, ko = case
     q, k, v = _qkv(Sq, Sk, H, Hkv, D, torch.float32, 1)
-    out, lse = cp.cp_attn_block(q.cuda(), k.cuda(), v.cuda(), q_offset=qo, k_offset=ko,
-                                causal=causal)
+    out, out_ok = guarded((Sq, H, D), torch.float32)
+    lse, lse_ok = guarded((H, Sq), torch.float32)
+    cp.cp_attn_block(q.cuda(), k.cuda(), v.cuda(), q_offset=qo, k_offset=ko, causal=causal,
+                     out=out, lse=lse)
     cp.cp_check_device_error()
     ro, rl = oracle.attention(q.numpy(), k.numpy(), v.numpy(), causal=causal, q_offset=qo,
                               k_offset=ko)
     compare(out, lse, ro, rl, ATOL_F32, ATOL_F32)
+    assert out_ok() and lse_ok(), "write outside out / lse"
 
 
 BF16_CASES = [  # Sq, Sk, H, Hkv, D, causal, q_off, k_off
@@ -69,11 +72,14 @@ BF16_CASES = [  # Sq, Sk, H, Hkv, D, causal, q_off, k_off
 def test_block_bf16(cp, case, out_dtype):
     Sq, Sk, H, Hkv, D, causal, qo, ko = case
     q, k, v = _qkv(Sq, Sk, H, Hkv, D, torch.bfloat16, 2)
-    out, lse = cp.cp_attn_block(q.cuda(), k.cuda(), v.cuda(), q_offset=qo, k_offset=ko,
-                                causal=causal, out_dtype=out_dtype)
+    out, out_ok = guarded((Sq, H, D), out_dtype)
+    lse, lse_ok = guarded((H, Sq), torch.float32)
+    cp.cp_attn_block(q.cuda(), k.cuda(), v.cuda(), q_offset=qo, k_offset=ko, causal=causal,
+                     out=out, lse=lse)
     cp.cp_check_device_error()
     ro, rl = oracle.attention(host(q), host(k), host(v), causal=causal, q_offset=qo, k_offset=ko)
     compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+    assert out_ok() and lse_ok(), "write outside out / lse"
 
 
 def test_block_bf16_large_logits(cp):

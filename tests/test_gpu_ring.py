@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from context_causal_attention_attn_gb300.inputs import make_qkv, sample_rows
-from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, host
+from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, guarded, host
 
 pytestmark = pytest.mark.gpu
 
@@ -165,12 +165,12 @@ def test_ring_32k_zigzag_sampled(cp):
 
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 def test_ring_128k_sampled(cp, layout):
-    _sampled_check(cp, 131072, 32, 32, 8, layout, n_rows=256)
+    _sampled_check(cp, 131072, 32, 32, 8, layout)
 
 
 def test_ulysses_64k_gqa_sampled(cp):
     """S=65536, 32 query / 8 KV heads, P=8 (one KV head per virtual rank)."""
-    _sampled_check(cp, 65536, 32, 8, 8, "contiguous", n_rows=256, ulysses=True)
+    _sampled_check(cp, 65536, 32, 8, 8, "contiguous", ulysses=True)
 
 
 # ------------------------------------------------------------ Ulysses small
@@ -228,7 +228,7 @@ def test_lse_merge(cp, Sq, H, D):
     cp.cp_lse_merge(acc, lacc, torch.from_numpy(ob).cuda(), torch.from_numpy(lb).cuda())
     torch.cuda.synchronize()
     ro, rl = oracle.lse_merge(oa, la, ob, lb)
-    compare(acc, lacc, ro, rl, ATOL_F32 * 4, ATOL_F32 * 4)
+    compare(acc, lacc, ro, rl, ATOL_F32, ATOL_F32)
 
 
 def test_lse_merge_matches_split_attention(cp):
@@ -250,10 +250,13 @@ def test_lse_merge_matches_split_attention(cp):
                                         (5, 4, "zigzag"), (32, 4, "striped"), (60, 3, "striped")])
 def test_ring_fp32_ragged_and_striped(cp, S, P, layout):
     q, k, v = make_qkv(S, 4, 16, Hkv=2, seed=S + P)
-    out, lse = cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), P, layout)
+    out, out_ok = guarded((S, 4, 16), torch.float32)
+    lse, lse_ok = guarded((4, S), torch.float32)
+    cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), P, layout, out=out, lse=lse)
     cp.cp_check_device_error()
     ro, rl = oracle.attention(q.numpy(), k.numpy(), v.numpy())
     compare(out, lse, ro, rl, ATOL_F32, ATOL_F32)
+    assert out_ok() and lse_ok(), "write outside out / lse"
 
 
 @pytest.mark.parametrize("S,P,layout", [(1000, 4, "zigzag"), (1000, 4, "contiguous"),
@@ -262,10 +265,13 @@ def test_ring_fp32_ragged_and_striped(cp, S, P, layout):
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_ring_bf16_ragged_and_striped(cp, S, P, layout, out_dtype):
     q, k, v = make_qkv(S, 8, 128, Hkv=4, dtype=torch.bfloat16, seed=S + P)
-    out, lse = cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), P, layout, out_dtype=out_dtype)
+    out, out_ok = guarded((S, 8, 128), out_dtype)
+    lse, lse_ok = guarded((8, S), torch.float32)
+    cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), P, layout, out=out, lse=lse)
     cp.cp_check_device_error()
     ro, rl = oracle.ring_forward(host(q), host(k), host(v), P, layout)[:2]
     compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+    assert out_ok() and lse_ok(), "write outside out / lse"
 
 
 def test_ring_32k_striped_sampled(cp):
@@ -489,12 +495,14 @@ def test_ring_host_ragged(cp, S, layout, out_dtype):
     q, k, v = make_qkv(S, H, D, Hkv=4, dtype=torch.bfloat16, seed=17)
     ref_out, ref_lse = cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), P, layout,
                                           out_dtype=out_dtype)
-    hout, hlse = cp.cp_ring_forward_host(*(t.pin_memory() for t in (q, k, v)), P, layout,
-                                         out_dtype=out_dtype, groups=2,
-                                         copy_stream=torch.cuda.Stream())
+    hout, out_ok = guarded((S, H, D), out_dtype, pin=True)
+    hlse, lse_ok = guarded((H, S), torch.float32, pin=True)
+    cp.cp_ring_forward_host(*(t.pin_memory() for t in (q, k, v)), P, layout, hout=hout,
+                            hlse=hlse, groups=2, copy_stream=torch.cuda.Stream())
     torch.cuda.current_stream().synchronize()
     cp.cp_check_device_error()
     assert torch.equal(hout, ref_out.cpu()) and torch.equal(hlse, ref_lse.cpu())
+    assert out_ok() and lse_ok(), "write outside the host out / lse"
 
 
 # --------------------------------------------------------- host-buffer Ulysses
@@ -528,3 +536,36 @@ def test_usp_host_equals_device(cp, layout, Hkv):
     torch.cuda.current_stream().synchronize()
     cp.cp_check_device_error()
     assert torch.equal(hout, ref_out.cpu()) and torch.equal(hlse, ref_lse.cpu())
+
+
+@pytest.mark.parametrize("H,Hkv,P,out_dtype", [(8, 4, 4, torch.float32),
+                                                (8, 2, 4, torch.bfloat16),
+                                                (32, 8, 8, torch.bfloat16)])
+def test_ulysses_host_against_oracle(cp, H, Hkv, P, out_dtype):
+    """cp_ulysses_forward_host against the oracle's Ulysses forward on every
+    row (P dividing Hkv, P a multiple of Hkv, and the 64K config's head
+    shape at S=1024)."""
+    S, D = 1024, 128
+    q, k, v = make_qkv(S, H, D, Hkv=Hkv, dtype=torch.bfloat16, seed=41 + P + Hkv)
+    hout, hlse = cp.cp_ulysses_forward_host(*(t.pin_memory() for t in (q, k, v)), P,
+                                            out_dtype=out_dtype,
+                                            copy_stream=torch.cuda.Stream())
+    torch.cuda.current_stream().synchronize()
+    cp.cp_check_device_error()
+    ro, rl = oracle.ulysses_forward(host(q), host(k), host(v), P)
+    compare(hout, hlse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+
+
+@pytest.mark.parametrize("layout,Hkv,Pu,Pr,out_dtype", [("zigzag", 4, 4, 2, torch.bfloat16),
+                                                        ("striped", 2, 4, 2, torch.float32),
+                                                        ("contiguous", 8, 2, 3, torch.bfloat16)])
+def test_usp_host_against_oracle(cp, layout, Hkv, Pu, Pr, out_dtype):
+    """cp_usp_forward_host against the oracle's USP forward on every row."""
+    S, H, D = 1020 if layout == "contiguous" else 1024, 8, 128
+    q, k, v = make_qkv(S, H, D, Hkv=Hkv, dtype=torch.bfloat16, seed=51 + Pu + Pr)
+    hout, hlse = cp.cp_usp_forward_host(*(t.pin_memory() for t in (q, k, v)), Pu, Pr, layout,
+                                        out_dtype=out_dtype, copy_stream=torch.cuda.Stream())
+    torch.cuda.current_stream().synchronize()
+    cp.cp_check_device_error()
+    ro, rl = oracle.usp_forward(host(q), host(k), host(v), Pu, Pr, layout)
+    compare(hout, hlse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)

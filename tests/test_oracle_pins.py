@@ -144,6 +144,31 @@ def test_closed_forms():
     assert pin_closed_forms() < 1e-12
 
 
+# ------------------------------------------------------------ sampled rows
+def pin_sampled_rows():
+    """The sampled-row path every long GPU test relies on: rows given as
+    positions (unsorted, first and last included), evaluated in small row
+    blocks so each block truncates the keys at its own largest position.
+    Checked against torch's float64 SDPA of the whole sequence (out) and the
+    brute-force-pinned full oracle (lse) at those rows."""
+    worst = 0.0
+    S, H, Hkv, D = 300, 4, 2, 16
+    q, k, v = _rand((S, H, D), 111), _rand((S, Hkv, D), 112), _rand((S, Hkv, D), 113)
+    rng = np.random.default_rng(114)
+    rows = np.concatenate([rng.choice(np.arange(1, S - 1), 40, replace=False), [S - 1, 0]])
+    rng.shuffle(rows)
+    ref_out = _sdpa(q, k, v, True)[rows]
+    ref_lse = oracle.attention(q, k, v, causal=True)[1][:, rows]
+    for got in (oracle.attention_monolithic(q, k, v, rows=rows),
+                oracle.attention(q[rows], k, v, causal=True, q_positions=rows, row_block=7)):
+        worst = max(worst, np.max(np.abs(got[0] - ref_out)), np.max(np.abs(got[1] - ref_lse)))
+    return worst
+
+
+def test_sampled_rows():
+    assert pin_sampled_rows() < 1e-12
+
+
 def test_fully_masked_rows():
     q, k, v = _rand((4, 2, 4), 5), _rand((6, 2, 4), 6), _rand((6, 2, 4), 7)
     o, l = oracle.attention(q, k, v, causal=True, q_offset=0, k_offset=2)
@@ -367,7 +392,7 @@ def _caught(*pins):
     return False
 
 
-ALL_PINS = (pin_brute_force, pin_sdpa, pin_closed_forms, pin_merge_identity,
+ALL_PINS = (pin_brute_force, pin_sdpa, pin_closed_forms, pin_sampled_rows, pin_merge_identity,
             pin_ring_equals_monolithic, pin_ulysses, pin_permute)
 
 

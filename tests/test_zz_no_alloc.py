@@ -12,8 +12,9 @@ process and after the rest of the suite.
 import pytest
 import torch
 
+import oracle
 from context_causal_attention_attn_gb300.inputs import make_qkv
-from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT
+from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, host
 
 
 @pytest.fixture(scope="module")
@@ -26,21 +27,42 @@ def cp():
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_version_twice(cp):
-    """Two calls in a row through the C ABI agree with cp_ring_forward (which
-    takes a caller workspace) within the bf16 tolerances of the suite."""
+    """Two calls in a row through the C ABI give the bits of cp_ring_forward
+    (which takes a caller workspace; both run the same launches), so they are
+    also within the suite's bf16 tolerances; the first call is also checked
+    against the oracle on every row."""
     S, H, D, P = 4096, 32, 128, 4
     q, k, v = make_qkv(S, H, D, dtype=torch.bfloat16, device="cuda", seed=3)
     ref_out, ref_lse = cp.cp_ring_forward(q, k, v, P, "zigzag", out_dtype=torch.bfloat16)
     cp.cp_check_device_error()
-    for _ in range(2):
-        out = torch.empty_like(ref_out)
-        lse = torch.empty_like(ref_lse)
+    for call in range(2):
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
         cp.cp_ring_forward_noalloc(q, k, v, P, "zigzag", out=out, lse=lse)
         cp.cp_check_device_error()
         d_out = (out.float() - ref_out.float()).abs().max().item()
         d_lse = (lse - ref_lse).abs().max().item()
         assert d_out <= ATOL_BF16_OUT and d_lse <= ATOL_BF16_LSE, (d_out, d_lse)
-        assert torch.isfinite(out.float()).all()
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse), call
+        if call == 0:
+            ro, rl = oracle.attention(host(q), host(k), host(v))
+            compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+
+
+@pytest.mark.gpu
+def test_noalloc_fp32_output_uses_no_scratch(cp):
+    """With an fp32 output the output is the accumulator: no scratch is
+    looked up and the call equals cp_ring_forward (the handbook's toy, fp32,
+    atol 1e-5 against the oracle)."""
+    q, k, v = (t.cuda() for t in make_qkv(32, 8, 16))
+    ref_out, ref_lse = cp.cp_ring_forward(q, k, v, 4, "contiguous")
+    for _ in range(2):
+        out, lse = cp.cp_ring_forward_noalloc(q, k, v, 4, "contiguous")
+        cp.cp_check_device_error()
+        assert out.dtype == torch.float32
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+        ro, rl = oracle.attention(host(q), host(k), host(v))
+        compare(out, lse, ro, rl, ATOL_F32, ATOL_F32)
 
 
 @pytest.mark.gpu
