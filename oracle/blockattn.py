@@ -57,16 +57,22 @@ def _row_lse_and_weights(s):
     """lse and softmax weights of each row of s (float64, -inf = masked).
 
     lse = m + log(sum exp(s - m)) with m the row max; rows whose entries are
-    all -inf give lse = -inf and all-zero weights.
+    all -inf give lse = -inf and all-zero weights.  Non-finite scores follow
+    the page's logsumexp / exp(s - lse): a NaN score makes the row NaN; a
+    +inf score makes lse +inf and the weights exp(inf - inf) = NaN.
     """
     m = np.max(s, axis=1) if s.shape[1] > 0 else np.full(s.shape[0], NEG_INF)
-    empty = ~np.isfinite(m)
-    m_safe = np.where(empty, 0.0, m)
-    e = np.exp(s - m_safe[:, None])
-    tot = np.sum(e, axis=1)
-    with np.errstate(divide="ignore"):
+    empty = m == NEG_INF
+    pinf = m == np.inf
+    m_safe = np.where(empty | pinf, 0.0, m)
+    with np.errstate(invalid="ignore", over="ignore"):
+        e = np.exp(s - m_safe[:, None])
+        tot = np.sum(e, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
         lse = np.where(empty, NEG_INF, m_safe + np.log(np.where(empty, 1.0, tot)))
-    w = np.where(empty[:, None], 0.0, e / np.where(empty, 1.0, tot)[:, None])
+        lse = np.where(pinf, np.inf, lse)
+        w = np.where(empty[:, None], 0.0, e / np.where(empty, 1.0, tot)[:, None])
+    w = np.where(pinf[:, None], np.nan, w)
     return lse, w
 
 

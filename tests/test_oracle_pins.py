@@ -177,6 +177,26 @@ def test_fully_masked_rows():
     assert np.all(np.isfinite(l[:, 2:])) and np.all(np.isfinite(o))
 
 
+def test_nonfinite_scores_follow_logsumexp():
+    """A key row of +inf (scores +inf or -inf by the sign of q) and a NaN
+    query: lse and out as the page's torch.logsumexp and exp(s - lse) @ v
+    give them in float64, row by row (masked keys are -inf, not NaN)."""
+    S, H, D = 6, 1, 4
+    q, k, v = _rand((S, H, D), 13), _rand((S, H, D), 14), _rand((S, H, D), 15)
+    k[2, 0, 1] = np.inf
+    q[4, 0, 3] = np.nan
+    o, l = oracle.attention(q, k, v, causal=True)
+    qt, kt, vt = (torch.from_numpy(a[:, 0, :]) for a in (q, k, v))
+    s = (qt @ kt.T) / math.sqrt(D)
+    s = s.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), -math.inf)
+    ref_l = torch.logsumexp(s, dim=-1)
+    ref_o = torch.exp(s - ref_l[:, None]) @ vt
+    assert np.array_equal(l[0], ref_l.numpy(), equal_nan=True)
+    assert np.allclose(o[:, 0, :], ref_o.numpy(), rtol=0, atol=1e-12, equal_nan=True)
+    assert np.isnan(l[0, 4]) and np.all(np.isnan(o[4, 0]))
+    assert np.all(np.isfinite(l[0, :2])), "rows before the infinite key are unaffected"
+
+
 def test_shift_invariance_of_offsets():
     q, k, v = _rand((9, 2, 4), 8), _rand((9, 2, 4), 9), _rand((9, 2, 4), 10)
     a = oracle.attention(q, k, v, q_offset=3, k_offset=1)
