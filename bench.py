@@ -3,9 +3,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      (the fp64 CPU oracle, timed)
 
-One step = one full ring forward over the sequence (all P virtual-rank steps,
-one kernel launch each, LSE merge fused into the attention epilogue) on
-inputs already resident in HBM.  Prints ONE JSON line on rank 0.
+One step = one full ring forward over the sequence (all P virtual-rank steps)
+through cp_ring_forward, on inputs already resident in HBM: for bf16 rings in
+the contiguous or zigzag layout all steps run in one launch (each query tile
+walks its rank's held KV chunks in step order and merges on chip); the
+_steps workloads and the striped layout run one launch per step with the LSE
+merge in the attention epilogue.  Prints ONE JSON line on rank 0.
 
 Workloads (synthetic, seeded N(0,1) inputs, the handbook's make_qkv recipe):
   ring128k_zigzag (default)  S=131072 H=32 D=128 bf16, P=8 zigzag
@@ -15,6 +18,7 @@ Workloads (synthetic, seeded N(0,1) inputs, the handbook's make_qkv recipe):
                              double buffers on a second stream (copy-mode ring)
   ring32k_zigzag             S=32768, P=8 zigzag
   ring4k_zigzag              S=4096, P=4 zigzag
+  ring*_zigzag_steps         the same rings, one launch per step (cp_ring_forward_steps)
   ulysses64k                 S=65536, 32 q / 8 kv heads, P=8 Ulysses
   usp64k                     the same shapes, Ulysses over 4 head groups x zigzag ring of 2
   lse_merge128k              the stand-alone LSE merge over S=131072, H=32, D=128 fp32 (GB/s)
@@ -50,6 +54,13 @@ WORKLOADS = {
                                  layout="zigzag"),
     "ring32k_zigzag": dict(kind="ring", S=32768, H=32, Hkv=32, D=128, P=8, layout="zigzag"),
     "ring4k_zigzag": dict(kind="ring", S=4096, H=32, Hkv=32, D=128, P=4, layout="zigzag"),
+    # the same rings as one launch per step, merging through the accumulator
+    "ring128k_zigzag_steps": dict(kind="ring_steps", S=131072, H=32, Hkv=32, D=128, P=8,
+                                  layout="zigzag"),
+    "ring32k_zigzag_steps": dict(kind="ring_steps", S=32768, H=32, Hkv=32, D=128, P=8,
+                                 layout="zigzag"),
+    "ring4k_zigzag_steps": dict(kind="ring_steps", S=4096, H=32, Hkv=32, D=128, P=4,
+                                layout="zigzag"),
     "ulysses64k": dict(kind="ulysses", S=65536, H=32, Hkv=8, D=128, P=8, layout="ulysses"),
     "usp64k": dict(kind="usp", S=65536, H=32, Hkv=8, D=128, P=8, Pu=4, Pr=2, layout="zigzag"),
     # backward (gradients of the ring forward) and a training step (forward + backward)
@@ -366,14 +377,21 @@ def run_gpu(args, wl, rank, world, local):
     out = torch.empty(S, H, D, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(H, S, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    if wl["kind"] == "ring":
+    ring_impl = None
+    if wl["kind"] in ("ring", "ring_steps"):
         ws = torch.empty(max(cp.cp_ring_workspace_size(S, H, D, torch.bfloat16), 16),
                          dtype=torch.uint8, device=dev)
-        launches_per_step = P
-        attn_stages = set(range(P))  # every launch is a ring step
+        one_launch = wl["kind"] == "ring" and cp.ring_runs_fused(q, layout)
+        launches_per_step = 1 if one_launch else P
+        attn_stages = set(range(launches_per_step))  # every launch is attention
+        ring_fn = cp.cp_ring_forward if wl["kind"] == "ring" else cp.cp_ring_forward_steps
+        ring_impl = (f"cp_ring_forward: all {P} steps in one launch (each query tile walks its "
+                     "rank's held KV chunks in step order, merging on chip)" if one_launch else
+                     f"{ring_fn.__name__}: one launch per step ({P}), each merging into the "
+                     "fp32 accumulator in its epilogue")
 
         def step():
-            cp.cp_ring_forward(q, k, v, P, layout, out=out, lse=lse, workspace=ws, stream=stream)
+            ring_fn(q, k, v, P, layout, out=out, lse=lse, workspace=ws, stream=stream)
     elif wl["kind"] == "ring_copy":
         ws = torch.empty(cp.cp_ring_copy_workspace_size(S, H, Hkv, D, P, layout, torch.bfloat16,
                                                         torch.bfloat16), dtype=torch.uint8,
@@ -469,7 +487,7 @@ def run_gpu(args, wl, rank, world, local):
     h2d_gbs, d2h_gbs, link_bytes = link_gbs(q, hq, stream)
     q.copy_(hq)
     K_e2e = max(1, min(K, 3))
-    host_api = wl["kind"] in ("ring", "ulysses", "usp")
+    host_api = wl["kind"] in ("ring", "ring_steps", "ulysses", "usp")
     host_fn = {"ulysses": "cp_ulysses_forward_host", "usp": "cp_usp_forward_host"}.get(
         wl["kind"], "cp_ring_forward_host")
     if wl["kind"] == "usp":
@@ -556,7 +574,8 @@ def run_gpu(args, wl, rank, world, local):
                    "layout": layout, "in_dtype": "bf16", "out_dtype": "bf16",
                    "accumulate": "fp32", "causal": True,
                    "l2": f"inputs larger than L2 ({(h2d >> 20)} MiB of q/k/v per rank)",
-                   "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+                   "flops_per_step": flops, "parallelism": f"replicas x{world}",
+                   **({"ring_impl": ring_impl} if ring_impl else {})},
         "tokens_per_s": round(world * S * K / (t_max_ms / 1e3), 1),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
@@ -575,13 +594,14 @@ def run_gpu(args, wl, rank, world, local):
                               "the allocator put them")},
     }
     peaks, peak_kind = load_peaks()
-    if wl["kind"] in ("ring", "ring_copy"):
+    ring_kinds = ("ring", "ring_steps", "ring_copy")
+    if wl["kind"] in ring_kinds:
         # every launch on the compute stream is the attention kernel (99.8% of
         # device time in the launch list); launches run back to back (copy
         # mode: the mean includes any wait for the KV copies)
-        per_launch = [total_ms / (K * P)] * (K * P)
-        attn_stages = set(range(P))
-    if (staged or wl["kind"] in ("ring", "ring_copy")) and per_launch:
+        per_launch = [total_ms / (K * launches_per_step)] * (K * launches_per_step)
+        attn_stages = set(range(launches_per_step))
+    if (staged or wl["kind"] in ring_kinds) and per_launch:
         mean_launch_ms = statistics.fmean(per_launch)
         achieved = flops / len(attn_stages) / (mean_launch_ms / 1e3) / 1e12
         peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -594,14 +614,17 @@ def run_gpu(args, wl, rank, world, local):
                      f"inside a multi-second loop); achieved = causal FLOPs per attention "
                      f"launch (flops_per_step / {len(attn_stages)} launches per step) / mean "
                      f"launch time ({mean_launch_ms:.3f} ms over {len(per_launch)} launches; "
-                     + ("the ring's launches overlap under programmatic dependent launch, so "
-                        "the mean is the step time / launches)" if wl["kind"] == "ring" else
+                     + ("the whole ring is one launch, so the mean is the step time)"
+                        if wl["kind"] == "ring" and launches_per_step == 1 else
+                        "the ring's launches overlap under programmatic dependent launch, so "
+                        "the mean is the step time / launches)" if wl["kind"] in ring_kinds[:2] else
                         "step time / launches, including waits for the KV copies on the side "
                         "stream)" if wl["kind"] == "ring_copy" else
                         "each launch bracketed by events, permute launches excluded)"))}
     else:
         result["roofline"] = None
-    if wl["kind"] == "ring" and layout in ("contiguous", "zigzag") and S % (2 * P) == 0:
+    if wl["kind"] in ("ring", "ring_steps") and layout in ("contiguous", "zigzag") and \
+            S % (2 * P) == 0:
         per, imb = per_rank_times(cp, q, k, v, P, layout, stream)
         result["per_virtual_rank_ms"] = per
         result["virtual_rank_imbalance"] = imb
@@ -681,12 +704,19 @@ def run_bwd(args, wl, rank, world, local):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     bws = torch.empty(cp.cp_ring_backward_workspace_size(S, H, Hkv, D, torch.bfloat16),
                       dtype=torch.uint8, device=dev)
-    launches = ([("fwd", t) for t in range(P)] if train else []) + [("delta", -1)] + [
+    # the forward of a training step: cp_ring_forward (one launch for the whole
+    # ring where it runs fused, else one per step)
+    fwd_launches = [("fwd", -1)] if cp.ring_runs_fused(q, layout) else [
+        ("fwd", t) for t in range(P)]
+    launches = (fwd_launches if train else []) + [("delta", -1)] + [
         ("dkdv" if l % 2 == 0 else "dq", l) for l in range(2 * P)]
 
     def launch(kind, l, tensors=(q, k, v, do)):
         q_, k_, v_, do_ = tensors
-        if kind == "fwd":
+        if kind == "fwd" and l < 0:
+            cp.cp_ring_forward(q_, k_, v_, P, layout, out=out, lse=lse, workspace=fws,
+                               stream=stream)
+        elif kind == "fwd":
             cp.cp_ring_step(q_, k_, v_, P, layout, l, out, lse, fws, stream=stream)
         else:
             cp.cp_ring_backward_step(q_, k_, v_, out, do_, lse, P, layout, l, dq, dk, dv, bws,

@@ -54,6 +54,10 @@ def lib():
                                   vp, vp]),
         "cp_ring_forward_noalloc": (i32, [vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp,
                                           i32, vp, vp]),
+        "cp_ring_forward_fused": (i32, [vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp, i32,
+                                        vp, vp]),
+        "cp_ring_forward_steps": (i32, [vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp, i32,
+                                        vp, vp, vp]),
         "cp_ring_copy_workspace_size": (i64, [i64, i32, i32, i32, i32, i32, i32, i32]),
         "cp_ring_forward_copy": (i32, [vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, vp, i32,
                                        vp, vp, vp, vp]),
@@ -209,16 +213,56 @@ def _ring_buffers(q, out, out_dtype, lse, workspace):
     return out, lse, workspace
 
 
+def ring_runs_fused(q, layout):
+    """Whether cp_ring_forward runs the ring in one launch (bf16 inputs,
+    contiguous or zigzag), which needs no workspace."""
+    return q.dtype == torch.bfloat16 and layout in ("contiguous", "zigzag")
+
+
 def cp_ring_forward(q, k, v, P, layout="zigzag", out=None, out_dtype=None, lse=None,
                     workspace=None, stream=None):
     """Ring attention of the whole sequence over P virtual ranks -> (out, lse)."""
     S, H, D = q.shape
     Hkv = k.shape[1]
+    if workspace is None and ring_runs_fused(q, layout):
+        workspace = torch.empty(0, dtype=torch.uint8, device=q.device)  # unused
     out, lse, workspace = _ring_buffers(q, out, out_dtype, lse, workspace)
     _dev(q, k, v, out, lse, workspace)
     _check(lib().cp_ring_forward(_ptr(q), _ptr(k), _ptr(v), _dt(q), S, H, Hkv, D, int(P),
                                  _layout(layout), _ptr(out), _dt(out), _ptr(lse), _ptr(workspace),
                                  _stream(stream)))
+    return out, lse
+
+
+def cp_ring_forward_steps(q, k, v, P, layout="zigzag", out=None, out_dtype=None, lse=None,
+                          workspace=None, stream=None):
+    """The ring as one launch per step, merging through the fp32
+    accumulator -> (out, lse)."""
+    S, H, D = q.shape
+    Hkv = k.shape[1]
+    out, lse, workspace = _ring_buffers(q, out, out_dtype, lse, workspace)
+    _dev(q, k, v, out, lse, workspace)
+    _check(lib().cp_ring_forward_steps(_ptr(q), _ptr(k), _ptr(v), _dt(q), S, H, Hkv, D, int(P),
+                                       _layout(layout), _ptr(out), _dt(out), _ptr(lse),
+                                       _ptr(workspace), _stream(stream)))
+    return out, lse
+
+
+def cp_ring_forward_fused(q, k, v, P, layout="zigzag", out=None, out_dtype=None, lse=None,
+                          stream=None):
+    """The ring with all P steps inside one launch (bf16 inputs, contiguous or
+    zigzag) -> (out, lse); needs no workspace."""
+    S, H, D = q.shape
+    Hkv = k.shape[1]
+    out_dtype = out_dtype or (out.dtype if out is not None else q.dtype)
+    if out is None:
+        out = torch.empty(S, H, D, dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(H, S, dtype=torch.float32, device=q.device)
+    _dev(q, k, v, out, lse)
+    _check(lib().cp_ring_forward_fused(_ptr(q), _ptr(k), _ptr(v), _dt(q), S, H, Hkv, D, int(P),
+                                       _layout(layout), _ptr(out), _dt(out), _ptr(lse),
+                                       _stream(stream)))
     return out, lse
 
 

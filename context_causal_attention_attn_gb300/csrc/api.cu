@@ -390,6 +390,70 @@ int ring_step_impl(const void* q, const void* k, const void* v, cp_dtype in_dt, 
   return launch_items(L, in_dt, q, q_rows, kk, vv, k_rows, stream, dependent);
 }
 
+// The ring in one launch (bf16 inputs, contiguous or zigzag layout): one
+// work item per (virtual rank r, own query chunk qc), whose key segments are
+// the chunks rank r holds at steps t = 0, 1, ..., P-1 (src = (r - t) mod P,
+// ascending within a step) that are not later than qc -- exactly the blocks
+// the per-step ring evaluates for those rows, in the same order.  Each query
+// tile carries its running max, sum and output in TMEM from one step to the
+// next (the online-softmax form of the LSE merge) and writes the final
+// result once, so no accumulator round trip, per-step epilogue or launch
+// separates the steps.
+int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int H, int Hkv,
+                    int D, int P, cp_layout layout, void* out, cp_dtype out_dt, float* lse,
+                    cudaStream_t stream) {
+  const int64_t nchunks = layout == CP_ZIGZAG ? 2 * P : P;
+  const int64_t C = (S + nchunks - 1) / nchunks;
+  auto chunk_rows = [&](int64_t c) -> int64_t {
+    return std::max<int64_t>(0, std::min<int64_t>(S, (c + 1) * C) - c * C);
+  };
+  Launch L;
+  fill_common(L.p, H, Hkv, D, 0.f, out_dt, out,
+              out_dt == CP_F32 ? static_cast<float*>(out) : nullptr, lse, S);
+  L.p.ring_C = C;
+  L.p.ring_S = S;
+  std::vector<int64_t> work;  // visible keys x rows, for the longest-first order
+  for (int r = 0; r < P; ++r) {
+    int qcs[2];
+    const int nq = rank_chunks(P, layout, r, qcs);
+    for (int a = 0; a < nq; ++a) {
+      const int qc = qcs[a];
+      if (chunk_rows(qc) == 0) continue;
+      WorkItem w{};
+      w.q_mem_row = qc * C;
+      w.q_pos = qc * C;
+      w.o_row = qc * C;
+      w.lse_col = qc * C;
+      w.sq = static_cast<int32_t>(chunk_rows(qc));
+      w.batch = 1;
+      w.flags = kFlagCausal | kFlagFinal;
+      int64_t keys = 0;
+      for (int t = 0; t < P; ++t) {
+        const int src = ((r - t) % P + P) % P;
+        int kcs[2];
+        const int nk = rank_chunks(P, layout, src, kcs);
+        for (int b = 0; b < nk; ++b) {
+          if (kcs[b] > qc || chunk_rows(kcs[b]) == 0) continue;
+          if (w.nchunk >= kMaxRingChunks) return fail(CP_ERR_ARG, "too many ring chunks");
+          w.chunk[w.nchunk++] = static_cast<uint8_t>(kcs[b]);
+          keys += kcs[b] == qc ? chunk_rows(qc) / 2 : chunk_rows(kcs[b]);
+        }
+      }
+      L.items.push_back(w);
+      work.push_back(keys * w.sq);
+    }
+  }
+  // longest items first (the grid is scheduled roughly in order)
+  std::vector<size_t> order(L.items.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](size_t a, size_t b) { return work[a] > work[b]; });
+  std::vector<WorkItem> sorted;
+  for (size_t i : order) sorted.push_back(L.items[i]);
+  L.items.swap(sorted);
+  return launch_items(L, CP_BF16, q, S, k, v, S, stream);
+}
+
 // Copy-mode ring: one D2D copy per rank and tensor moves every rank's held
 // KV into rank+1's other buffer on `copy_stream` while step t computes.
 int ring_forward_copy_impl(const void* q, const void* k, const void* v, cp_dtype in_dt, int64_t S,
@@ -700,6 +764,12 @@ namespace cpattn {
 // Lets other translation units of the library report an error through
 // cp_last_error() of the calling thread.
 int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+// Whether cp_ring_forward (and the host-buffer ring) run all steps in one
+// launch: bf16 inputs (tensor-core path) in the contiguous or zigzag layout.
+bool ring_runs_fused(cp_dtype in_dt, cp_layout layout) {
+  return in_dt == CP_BF16 && (layout == CP_CONTIGUOUS || layout == CP_ZIGZAG);
+}
 }  // namespace cpattn
 
 // =================================================================== C ABI
@@ -807,11 +877,53 @@ int cp_ring_step(const void* q, const void* k, const void* v, cp_dtype in_dt, in
                            workspace, stream, false);
 }
 
+static int ring_fused_checked(const void* q, const void* k, const void* v, cp_dtype in_dt,
+                              int64_t S, int H, int Hkv, int D, int P, cp_layout layout, void* out,
+                              cp_dtype out_dt, float* lse, cp_stream_t stream) {
+  int rc = check_ring(in_dt, S, H, Hkv, D, P, layout, out_dt);
+  if (rc != CP_OK) return rc;
+  if (in_dt != CP_BF16)
+    return fail(CP_ERR_DTYPE, "the one-launch ring needs bf16 inputs (tensor-core path)");
+  if (layout == CP_STRIPED)
+    return fail(CP_ERR_ARG, "the one-launch ring takes the contiguous or zigzag layout");
+  if (!q || !k || !v || !out || !lse) return fail(CP_ERR_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(CP_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3) != 0)
+    return fail(CP_ERR_ALIGN, "lse must be 4-byte aligned");
+  rc = ring_fused_impl(q, k, v, S, H, Hkv, D, P, layout, out, out_dt, lse,
+                       reinterpret_cast<cudaStream_t>(stream));
+  return rc == CP_OK ? ok() : rc;
+}
+
+int cp_ring_forward_fused(const void* q, const void* k, const void* v, cp_dtype in_dt, int64_t S,
+                          int H, int Hkv, int D, int P, cp_layout layout, void* out,
+                          cp_dtype out_dt, float* lse, cp_stream_t stream) {
+  return ring_fused_checked(q, k, v, in_dt, S, H, Hkv, D, P, layout, out, out_dt, lse, stream);
+}
+
+int cp_ring_forward_steps(const void* q, const void* k, const void* v, cp_dtype in_dt, int64_t S,
+                          int H, int Hkv, int D, int P, cp_layout layout, void* out,
+                          cp_dtype out_dt, float* lse, void* workspace, cp_stream_t stream) {
+  int rc = check_ring(in_dt, S, H, Hkv, D, P, layout, out_dt);
+  if (rc != CP_OK) return rc;
+  for (int t = 0; t < P; ++t) {
+    rc = ring_step_checked(q, k, v, in_dt, S, H, Hkv, D, P, layout, t, out, out_dt, lse,
+                           workspace, stream, t > 0);
+    if (rc != CP_OK) return rc;
+  }
+  return ok();
+}
+
 int cp_ring_forward(const void* q, const void* k, const void* v, cp_dtype in_dt, int64_t S, int H,
                     int Hkv, int D, int P, cp_layout layout, void* out, cp_dtype out_dt,
                     float* lse, void* workspace, cp_stream_t stream) {
   int rc = check_ring(in_dt, S, H, Hkv, D, P, layout, out_dt);
   if (rc != CP_OK) return rc;
+  // the tensor-core path runs the steps in one launch (measured faster at
+  // every length: no per-step epilogue, accumulator round trip or launch)
+  if (ring_runs_fused(in_dt, layout))
+    return ring_fused_checked(q, k, v, in_dt, S, H, Hkv, D, P, layout, out, out_dt, lse, stream);
   for (int t = 0; t < P; ++t) {
     rc = ring_step_checked(q, k, v, in_dt, S, H, Hkv, D, P, layout, t, out, out_dt, lse,
                            workspace, stream, t > 0);
@@ -1010,10 +1122,15 @@ int cp_ring_forward_host(const void* hq, const void* hk, const void* hv, cp_dtyp
     char* dv = ws + st.v + g * kg;
     char* dout = ws + st.out + g * og;
     float* dlse = reinterpret_cast<float*>(ws + st.lse + g * lg);
-    for (int t = 0; t < P; ++t) {
-      rc = ring_step_impl(dq, dk, dv, in_dt, S, Hg, Hkg, D, P, layout, t, dout, out_dt, dlse,
-                          ws + st.acc, cs, nullptr, nullptr, t > 0);
+    if (ring_runs_fused(in_dt, layout)) {
+      rc = ring_fused_impl(dq, dk, dv, S, Hg, Hkg, D, P, layout, dout, out_dt, dlse, cs);
       if (rc != CP_OK) return rc;
+    } else {
+      for (int t = 0; t < P; ++t) {
+        rc = ring_step_impl(dq, dk, dv, in_dt, S, Hg, Hkg, D, P, layout, t, dout, out_dt, dlse,
+                            ws + st.acc, cs, nullptr, nullptr, t > 0);
+        if (rc != CP_OK) return rc;
+      }
     }
     pl.compute_end(g);
     pl.out(static_cast<char*>(hout) + g * o_w, dout, o_w, o_pitch, S);

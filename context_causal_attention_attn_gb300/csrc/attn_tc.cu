@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include "attn_fwd_common.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -52,14 +53,6 @@ namespace cpattn {
 using namespace sm100;
 
 namespace tc {
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int HD = 128;
-constexpr uint32_t TILE_BYTES = BM * HD * 2;  // 32768
-constexpr uint32_t BOX_BYTES = BM * 64 * 2;   // 16384: rows x 64 columns
-constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
-constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
-
 // NT query tiles per CTA (built: NT = 1, two CTAs per SM with 256 TMEM
 // columns and a 2-stage ring each; NT = 2 would own the SM with 512 columns
 // and a 4-stage ring).
@@ -99,53 +92,6 @@ struct Cfg {
                 "staging = Q + K/V stage 0");
 };
 }  // namespace tc
-
-__device__ __forceinline__ int seg_tiles(const KSeg& s) { return (s.len + tc::BN - 1) / tc::BN; }
-
-// Number of KV tiles, in segment order, holding at least one key visible to a
-// query at position qp_last.  Positions grow along the tile order, so the
-// visible tiles of any query form a prefix of that order.
-__device__ __forceinline__ int visible_tiles(const WorkItem& it, int64_t qp_last, bool causal) {
-  int n = 0;
-  for (int s = 0; s < it.nseg; ++s) {
-    const int T = seg_tiles(it.seg[s]);
-    if (!causal) {
-      n += T;
-      continue;
-    }
-    if (qp_last < it.seg[s].pos) break;
-    const int64_t v = (qp_last - it.seg[s].pos) / tc::BN + 1;
-    if (v < T) {
-      n += static_cast<int>(v);
-      break;
-    }
-    n += T;
-  }
-  return n;
-}
-
-// Tile j of the concatenated segments -> (first key row in memory, first key
-// position, keys in the tile).
-__device__ __forceinline__ void tile_keys(const WorkItem& it, int j, int64_t& mem_row,
-                                          int64_t& pos, int& nk) {
-  const int T0 = it.nseg > 0 ? seg_tiles(it.seg[0]) : 0;
-  const int s = j < T0 ? 0 : 1;
-  const int t = j < T0 ? j : j - T0;
-  mem_row = it.seg[s].mem_row + static_cast<int64_t>(t) * tc::BN;
-  pos = it.seg[s].pos + static_cast<int64_t>(t) * tc::BN;
-  nk = min(tc::BN, it.seg[s].len - t * tc::BN);
-}
-
-// Stripe r of the keys of tile j.
-__device__ __forceinline__ int tile_stripe(const WorkItem& it, int j) {
-  const int T0 = it.nseg > 0 ? seg_tiles(it.seg[0]) : 0;
-  return it.seg[j < T0 ? 0 : 1].stripe;
-}
-
-__device__ __forceinline__ void record_timeout(int* dev_err, volatile int* abort_flag) {
-  *abort_flag = 1;
-  atomicCAS(dev_err, 0, kDevErrTimeout);
-}
 
 // kStriped: rows are addressed as stripes (4-D maps, strided output rows);
 // otherwise plain rows with 3-D maps, and those terms fold away.
@@ -196,8 +142,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
   const int64_t k_boff = static_cast<int64_t>(b) * it.b_k_rows;
   const int nrows_a = min(tc::BM, it.sq - row0);
   const int nrows_b = NT == 2 ? max(0, min(tc::BM, it.sq - row0 - tc::BM)) : 0;
-  const int n_a = visible_tiles(it, q_pos0 + nrows_a - 1, causal);
-  const int n_b = nrows_b > 0 ? visible_tiles(it, q_pos0 + tc::BM + nrows_b - 1, causal) : 0;
+  const int n_a = visible_tiles(it, p, q_pos0 + nrows_a - 1, causal);
+  const int n_b = nrows_b > 0 ? visible_tiles(it, p, q_pos0 + tc::BM + nrows_b - 1, causal) : 0;
   const int nkv = max(n_a, n_b);
 
   // ---------------------------------------------------------------- setup
@@ -207,13 +153,15 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
   const bool producer = warp == C::WARP_LOAD && lane == 0;
   uint64_t pol_q = 0, pol_kv = 0;
   int issued = 0;  // producer: K/V copies issued
+  TileCursor pcur;  // producer: the next tile to load
   // K_j and V_j into the next stages (n = 2 j + w), each once its stage is
-  // released; false when a wait expired
+  // released; false when a wait expired.  Called for j = 0, 1, ... in order.
   auto issue_kv = [&](int j) -> bool {
     int64_t kmem, kpos;
-    int nk;
-    tile_keys(it, j, kmem, kpos, nk);
-    const int kstripe = kStriped ? tile_stripe(it, j) : 0;
+    int nk, kstripe;
+    pcur.keys(it, p, kmem, kpos, nk, kstripe);
+    pcur.next(it, p, q_pos0 + nrows_a - 1, causal);
+    if (!kStriped) kstripe = 0;
     const int krow = static_cast<int>(kmem + k_boff);
     for (int w = 0; w < 2; ++w) {
       const int n = 2 * j + w;
@@ -256,6 +204,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
     tma_prefetch_desc(&tm_v);
     pol_q = policy_evict_first();
     pol_kv = policy_evict_last();
+    pcur.init(it, p, q_pos0 + nrows_a - 1, causal);
     const int ntiles_q = nrows_b > 0 ? 2 : 1;
     mbar_arrive_expect_tx(bar(C::BAR_Q), ntiles_q * tc::TILE_BYTES);
     for (int x = 0; x < ntiles_q; ++x)
@@ -445,6 +394,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         }
         if (row < nrows) cp_async4(sbase + C::OFF_LSE + row * 4, lse_addr());
       };
+      TileCursor cur;
+      cur.init(it, p, qp_first + nrows - 1, causal);
       for (int j = 0; j < nx; ++j) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(bar(C::BAR_S_FULL + x), j & 1,
                                                            tc::WAIT_LIMIT_NS, abort_flag));
@@ -465,8 +416,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         for (int c = 0; c < tc::BN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
         int64_t kmem, kpos;
-        int nk;
-        tile_keys(it, j, kmem, kpos, nk);
+        int nk, kstripe;
+        cur.keys(it, p, kmem, kpos, nk, kstripe);
+        cur.next(it, p, qp_first + nrows - 1, causal);
         const bool need_mask = nk < tc::BN || (causal && kpos + nk - 1 > qp_first);
         if (need_mask) {
           int64_t lim64 = causal ? min(static_cast<int64_t>(nk), qp - kpos + 1)

@@ -44,6 +44,7 @@ cudaError_t once_per_device(PerDeviceOnce& o, F&& fn) {
 
 constexpr int kMaxItems = 32;   // 2 items per virtual rank per ring step
 constexpr int kMaxSegs = 2;     // zigzag: a late query chunk sees 2 KV chunks
+constexpr int kMaxRingChunks = 32;  // chunks of a zigzag ring of 16 ranks
 
 // Item flags.
 constexpr int kFlagMerge = 1;   // merge into the fp32 accumulator (read acc, lse)
@@ -75,6 +76,12 @@ struct WorkItem {
   // per-batch strides: rows of q / k / out, heads of lse
   int64_t b_q_rows, b_k_rows, b_o_rows, b_lse_heads;
   KSeg seg[kMaxSegs];
+  // A whole ring walked in one launch (tensor-core path): when nchunk > 0
+  // the key segments are the sequence chunks chunk[0..nchunk) in the order
+  // the ring's steps reach them (chunk c = rows [c C, min(S, (c+1) C)) with
+  // C = AttnParams::ring_C, S = AttnParams::ring_S), and seg / nseg are unused.
+  int32_t nchunk;
+  uint8_t chunk[kMaxRingChunks];
 };
 
 struct AttnParams {
@@ -99,6 +106,7 @@ struct AttnParams {
   const void* k;
   const void* v;
   int64_t q_rows, k_rows;      // rows of the q / k tensors (bounds)
+  int64_t ring_C, ring_S;      // chunk rows and sequence length of chunk-list items
 };
 
 // Status word written by kernels whose bounded wait expired.

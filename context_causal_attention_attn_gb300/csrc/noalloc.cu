@@ -1,7 +1,8 @@
 // cp_ring_forward_noalloc: the ring forward for callers that may not
 // allocate device memory.
 //
-// cp_ring_forward with a bf16 output needs an fp32 accumulator of S*H*D
+// cp_ring_forward with a bf16 output, when it runs the ring step by step
+// (fp32 inputs, or the striped layout), needs an fp32 accumulator of S*H*D
 // floats as scratch, which the caller normally allocates and passes as the
 // workspace.  Some callers cannot do that: code that runs inside another
 // framework's fixed device-memory budget (an inference engine plugin whose
@@ -20,6 +21,7 @@
 
 namespace cpattn {
 int set_last_error(int code, const char* msg);
+bool ring_runs_fused(cp_dtype in_dt, cp_layout layout);
 }
 
 namespace {
@@ -60,8 +62,10 @@ extern "C" int cp_ring_forward_noalloc(const void* q, const void* k, const void*
                                        cp_layout layout, void* out, cp_dtype out_dt, float* lse,
                                        cp_stream_t stream) {
   // same validation and error reporting as the workspace version
-  const int64_t need = cp_ring_workspace_size(S, H, D, out_dt);
+  int64_t need = cp_ring_workspace_size(S, H, D, out_dt);
   if (need < 0) return static_cast<int>(need);
+  // a ring cp_ring_forward runs in one launch keeps no accumulator
+  if (cpattn::ring_runs_fused(in_dt, layout)) need = 0;
   if (static_cast<uint64_t>(need) > kScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),

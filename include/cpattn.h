@@ -128,7 +128,12 @@ int64_t cp_ring_workspace_size(int64_t S, int H, int D, cp_dtype out_dt);
  *   (received from rank r-1); it evaluates every (own query chunk, held KV
  *   chunk) pair in which some key precedes some query (for striped: every
  *   pair), merges the result into its running (out, lse) with the LSE merge,
- *   and skips the rest.  One kernel launch per step covers all ranks.
+ *   and skips the rest.
+ *   Execution: with bf16 inputs in the contiguous or zigzag layout all P
+ *   steps run inside one kernel launch (cp_ring_forward_fused; the workspace
+ *   is then unused); otherwise (fp32 inputs, striped layout) one launch per
+ *   step covers all ranks and merges into the accumulator
+ *   (cp_ring_forward_steps).
  *   out [S,H,D] out_dt, lse [H,S] fp32.  workspace: device memory of
  *   cp_ring_workspace_size() bytes (NULL allowed when that is 0).
  *   The result equals cp_attn_block over the whole sequence up to rounding.
@@ -138,6 +143,44 @@ int cp_ring_forward(const void* q, const void* k, const void* v, cp_dtype in_dt,
                     int64_t S, int H, int Hkv, int D, int P, cp_layout layout,
                     void* out, cp_dtype out_dt, float* lse, void* workspace,
                     cp_stream_t stream);
+
+/*
+ * cp_ring_forward_steps - the ring of cp_ring_forward as P kernel launches,
+ * one per step (every layout and dtype).  Launch t evaluates the blocks of
+ * step t for all virtual ranks and LSE-merges each into the fp32
+ * accumulator (the workspace, or out itself when out_dt = CP_F32) in its
+ * epilogue; the last step to touch a row writes it to out.  Launches after
+ * the first start while the previous one drains (programmatic dependent
+ * launch) and wait for it only before their epilogue.  Arguments as
+ * cp_ring_forward; same result up to rounding (bit for bit the result of
+ * cp_ring_step for t = 0 .. P-1).
+ */
+int cp_ring_forward_steps(const void* q, const void* k, const void* v, cp_dtype in_dt,
+                          int64_t S, int H, int Hkv, int D, int P, cp_layout layout,
+                          void* out, cp_dtype out_dt, float* lse, void* workspace,
+                          cp_stream_t stream);
+
+/*
+ * cp_ring_forward_fused - the ring of cp_ring_forward with all P steps
+ * inside one kernel launch.  [CP-handbook] sections "Ring Attention：KV 沿环
+ * 传一圈" and "之字形切分"; the running (max, sum, unnormalised output) form
+ * of the merge is [SP-CP-survey] section 3.2.
+ *
+ *   Every query tile of virtual rank r walks the KV chunks that rank holds at
+ *   steps 0, 1, ..., P-1 (src = (r - t) mod P), in that order, evaluating the
+ *   same (query chunk, held KV chunk) blocks as the per-step ring; instead of
+ *   writing each step's (out, lse) and merging it into an accumulator, it
+ *   carries the running max, sum and unnormalised output from one step to
+ *   the next on chip and writes (out, lse) once.  The result equals
+ *   cp_ring_forward_steps' up to rounding (the same terms merged in another
+ *   grouping).  bf16 inputs (D = 128) in the contiguous or zigzag layout
+ *   (other cases return CP_ERR_DTYPE / CP_ERR_ARG); any S, 1 <= P <=
+ *   CP_MAX_RANKS; no workspace.  Arguments otherwise as cp_ring_forward,
+ *   which takes this path for those inputs.
+ */
+int cp_ring_forward_fused(const void* q, const void* k, const void* v, cp_dtype in_dt,
+                          int64_t S, int H, int Hkv, int D, int P, cp_layout layout,
+                          void* out, cp_dtype out_dt, float* lse, cp_stream_t stream);
 
 /*
  * cp_ring_forward_noalloc - cp_ring_forward for callers that cannot
@@ -150,12 +193,14 @@ int cp_ring_forward(const void* q, const void* k, const void* v, cp_dtype in_dt,
  *   cudaFree would synchronise the device and stall other streams.
  *
  *   Same arguments, layout and results as cp_ring_forward, minus the
- *   workspace.  With out_dt = CP_BF16 the fp32 accumulator lives in a 64 MiB
- *   array inside the library (static device memory every GPU that loads the
- *   library holds until process exit), so S*H*D must be <= 16,777,216
- *   (S = 4096 at H = 32, D = 128); larger sizes return CP_ERR_SHAPE with a
- *   message.  With out_dt = CP_F32 no scratch is used at all.  The call
- *   allocates nothing.
+ *   workspace.  When cp_ring_forward runs the ring step by step (fp32
+ *   inputs, or the striped layout) with out_dt = CP_BF16, the fp32
+ *   accumulator lives in a 64 MiB array inside the library (static device
+ *   memory every GPU that loads the library holds until process exit), so
+ *   S*H*D must be <= 16,777,216 (S = 16384 at H = 8, D = 128); larger sizes
+ *   return CP_ERR_SHAPE with a message.  With out_dt = CP_F32, or for a ring
+ *   cp_ring_forward runs in one launch (bf16 inputs, contiguous or zigzag),
+ *   no scratch is used at all.  The call allocates nothing.
  *   The first call on a device looks up the array's device address (a
  *   one-time host set-up per device, done with that device current); make
  *   that first call before any stream capture.

@@ -66,3 +66,18 @@ def guarded(shape, dtype, device="cuda", guard_rows=2, pin=False):
     def intact():
         return bool((buf[:g] == SENTINEL).all()) and bool((buf[g + n:] == SENTINEL).all())
     return view, intact
+
+
+def ring_by_steps(cp, q, k, v, P, layout, out_dtype=None, stream=None):
+    """The per-step ring (cp_ring_step for t = 0 .. P-1 on one stream): the
+    bitwise reference of every entry point that runs the ring step by step
+    (copy mode, host buffers, sequences longer than the one-launch limit)."""
+    S, H, D = q.shape
+    out_dtype = out_dtype or q.dtype
+    out = torch.empty(S, H, D, dtype=out_dtype, device=q.device)
+    lse = torch.empty(H, S, dtype=torch.float32, device=q.device)
+    n = cp.cp_ring_workspace_size(S, H, D, out_dtype)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device) if n else None
+    for t in range(P):
+        cp.cp_ring_step(q, k, v, P, layout, t, out, lse, ws, stream=stream)
+    return out, lse

@@ -223,3 +223,28 @@ def test_product_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_header_constants_match_the_binding(cp):
+    text = open(HEADER).read()
+    for name in ("CP_MAX_RANKS",):
+        m = re.search(r"#define\s+" + name + r"\s+(\d+)", text)
+        assert m and int(m.group(1)) == getattr(cp, name), name
+
+
+def test_fused_ring_validation_without_gpu(cp):
+    """The one-launch ring takes bf16 inputs in the contiguous or zigzag
+    layout only; it rejects the rest before any device work."""
+    L = cp.lib()
+    F32, BF16 = cp.CP_F32, cp.CP_BF16
+    ptr = ctypes.c_void_p(256)
+    args = lambda in_dt, D, layout, P: (ptr, ptr, ptr, in_dt, 64, 4, 4, D, P, layout, ptr, BF16,
+                                        ptr, None)
+    assert L.cp_ring_forward_fused(*args(F32, 16, cp.CP_ZIGZAG, 2)) == -3
+    assert "bf16" in cp.cp_last_error()
+    assert L.cp_ring_forward_fused(*args(BF16, 128, cp.CP_STRIPED, 2)) == -1
+    assert L.cp_ring_forward_fused(*args(BF16, 128, cp.CP_ZIGZAG, 17)) == -1
+    assert L.cp_ring_forward_fused(*args(BF16, 64, cp.CP_ZIGZAG, 2)) == -2
+    bad = ctypes.c_void_p(258)
+    assert L.cp_ring_forward_fused(bad, ptr, ptr, BF16, 64, 4, 4, 128, 2, cp.CP_ZIGZAG, ptr,
+                                   BF16, ptr, None) == -4

@@ -24,7 +24,7 @@ import torch
 
 import oracle
 from context_causal_attention_attn_gb300.inputs import make_qkv
-from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, host
+from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, host, ring_by_steps
 
 pytestmark = pytest.mark.gpu
 NAN = float("nan")
@@ -118,16 +118,20 @@ def test_ring_bf16_nan_in_k_reaches_every_later_row(cp, layout):
     accumulator)."""
     S, H, Hkv, D, P = 1024, 4, 2, 128, 4
     q, k, v = (t.cuda() for t in make_qkv(S, H, D, Hkv=Hkv, dtype=torch.bfloat16, seed=63))
-    clean = cp.cp_ring_forward(q, k, v, P, layout, out_dtype=torch.bfloat16)
-    for j0 in (5, 600):
-        kd = k.clone()
-        kd[j0, 1, 0] = NAN
-        dirty = cp.cp_ring_forward(q, kd, v, P, layout, out_dtype=torch.bfloat16)
-        cp.cp_check_device_error()
-        no, nl = _masks(S, H, D)
-        no[j0:, 2:4, :] = True
-        nl[2:4, j0:] = True
-        _expect(clean, dirty, no, nl)
+    # cp_ring_forward (one launch at this length, except striped) and the
+    # per-step ring with its merges through the accumulator
+    for run in (lambda k_: cp.cp_ring_forward(q, k_, v, P, layout, out_dtype=torch.bfloat16),
+                lambda k_: ring_by_steps(cp, q, k_, v, P, layout, out_dtype=torch.bfloat16)):
+        clean = run(k)
+        for j0 in (5, 600):
+            kd = k.clone()
+            kd[j0, 1, 0] = NAN
+            dirty = run(kd)
+            cp.cp_check_device_error()
+            no, nl = _masks(S, H, D)
+            no[j0:, 2:4, :] = True
+            nl[2:4, j0:] = True
+            _expect(clean, dirty, no, nl)
 
 
 def test_ring_fp32_toy_nan_in_q(cp):

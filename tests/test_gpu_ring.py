@@ -12,7 +12,8 @@ import torch
 
 import oracle
 from context_causal_attention_attn_gb300.inputs import make_qkv, sample_rows
-from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, guarded, host
+from gpu_common import (ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, guarded, host,
+                        ring_by_steps)
 
 pytestmark = pytest.mark.gpu
 
@@ -67,11 +68,78 @@ def qkv4k():
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 def test_ring_4k_all_rows(cp, qkv4k, layout, out_dtype):
-    """S=4096, H=32, D=128, bf16, P=4: every row and head."""
+    """S=4096, H=32, D=128, bf16, P=4: every row and head, through
+    cp_ring_forward (all steps in one launch for bf16) and through the
+    per-step ring."""
     q, k, v, ro, rl = qkv4k
     out, lse = cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), 4, layout, out_dtype=out_dtype)
     cp.cp_check_device_error()
     compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+    fo, fl = cp.cp_ring_forward_fused(q.cuda(), k.cuda(), v.cuda(), 4, layout,
+                                      out_dtype=out_dtype)
+    assert torch.equal(fo, out) and torch.equal(fl, lse)
+    so, sl = ring_by_steps(cp, q.cuda(), k.cuda(), v.cuda(), 4, layout, out_dtype=out_dtype)
+    cp.cp_check_device_error()
+    compare(so, sl, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+
+
+# ------------------------------------------------- the ring in one launch
+@pytest.mark.parametrize("S,H,Hkv,P,layout", [(2048, 4, 2, 1, "zigzag"),
+                                              (2048, 4, 2, 2, "contiguous"),
+                                              (2048, 4, 4, 3, "zigzag"),
+                                              (2048, 8, 2, 8, "zigzag"),
+                                              (4096, 2, 2, 16, "zigzag"),
+                                              (4096, 2, 1, 16, "contiguous"),
+                                              (1000, 8, 4, 4, "zigzag"),    # 125-row chunks
+                                              (1000, 8, 4, 3, "contiguous"),
+                                              (300, 4, 2, 8, "zigzag"),     # 19-row chunks
+                                              (5, 2, 1, 4, "zigzag"),       # empty chunks
+                                              (129, 2, 2, 2, "contiguous")])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_ring_fused_against_oracle(cp, S, H, Hkv, P, layout, out_dtype):
+    """cp_ring_forward_fused (every step of the ring inside one launch, the
+    steps' blocks walked in ring order per query tile) against the oracle on
+    every row: degrees 1..16, GQA, chunk lengths that are not multiples of
+    the 128-key tile, a partial last chunk and empty chunks; guard bands
+    around out and lse."""
+    q, k, v = make_qkv(S, H, 128, Hkv=Hkv, dtype=torch.bfloat16, seed=S + P + H)
+    out, out_ok = guarded((S, H, 128), out_dtype)
+    lse, lse_ok = guarded((H, S), torch.float32)
+    cp.cp_ring_forward_fused(q.cuda(), k.cuda(), v.cuda(), P, layout, out=out, lse=lse)
+    cp.cp_check_device_error()
+    ro, rl = oracle.ring_forward(host(q), host(k), host(v), P, layout)[:2]
+    compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+    assert out_ok() and lse_ok(), "write outside out / lse"
+
+
+def test_ring_fused_32k_sampled(cp):
+    """The one-launch ring at S=32768, P=8 zigzag (every query tile walks up
+    to 256 KV tiles across the 8 steps), 512 seeded rows per head against the
+    oracle."""
+    S, H, P = 32768, 32, 8
+    q, k, v = make_qkv(S, H, 128, dtype=torch.bfloat16, device="cuda")
+    out, lse = cp.cp_ring_forward_fused(q, k, v, P, "zigzag")
+    cp.cp_check_device_error()
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+    C = S // (2 * P)
+    must = [c * C for c in range(2 * P)] + [c * C + C - 1 for c in range(2 * P)]
+    rows = sample_rows(S, 512, seed=1, must=must)
+    ro, rl = oracle.attention_monolithic(host(q), host(k), host(v), rows=rows)
+    compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE, rows=rows)
+
+
+def test_ring_fused_deterministic_and_close_to_steps(cp):
+    """Repeated one-launch rings give the same bits; the per-step ring (other
+    merge order of the same terms) agrees within the bf16 tolerances."""
+    S, H, P = 4096, 8, 4
+    q, k, v = make_qkv(S, H, 128, dtype=torch.bfloat16, seed=77, device="cuda")
+    a = cp.cp_ring_forward_fused(q, k, v, P, "zigzag", out_dtype=torch.float32)
+    b = cp.cp_ring_forward_fused(q, k, v, P, "zigzag", out_dtype=torch.float32)
+    s = ring_by_steps(cp, q, k, v, P, "zigzag", out_dtype=torch.float32)
+    cp.cp_check_device_error()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert (a[0] - s[0]).abs().max().item() <= ATOL_BF16_OUT
+    assert (a[1] - s[1]).abs().max().item() <= ATOL_BF16_LSE
 
 
 def test_ring_4k_block_equals_ring(cp, qkv4k):
@@ -88,7 +156,7 @@ def test_ring_steps_resume(cp, qkv4k):
     q, k, v, _, _ = qkv4k
     q, k, v = q.cuda(), k.cuda(), v.cuda()
     P, layout = 4, "zigzag"
-    ref_out, ref_lse = cp.cp_ring_forward(q, k, v, P, layout, out_dtype=torch.bfloat16)
+    ref_out, ref_lse = ring_by_steps(cp, q, k, v, P, layout, out_dtype=torch.bfloat16)
     out = torch.empty_like(ref_out)
     lse = torch.empty_like(ref_lse)
     ws = torch.empty(cp.cp_ring_workspace_size(4096, 32, 128, torch.bfloat16), dtype=torch.uint8,
@@ -111,13 +179,13 @@ def test_ring_steps_resume(cp, qkv4k):
                                               ("contiguous", torch.float32),
                                               ("striped", torch.bfloat16)])
 def test_ring_overlapped_steps_equal_separate_steps(cp, layout, out_dtype):
-    """cp_ring_forward launches steps 1..P-1 so that each overlaps the tail of
+    """cp_ring_forward_steps launches steps 1..P-1 so that each overlaps the tail of
     the step before; the result is bit for bit that of the steps launched
     one at a time (cp_ring_step), at 32K where many CTAs of consecutive steps
     run together."""
     S, H, D, P = 32768, 8, 128, 8
     q, k, v = make_qkv(S, H, D, dtype=torch.bfloat16, seed=21, device="cuda")
-    ref_out, ref_lse = cp.cp_ring_forward(q, k, v, P, layout, out_dtype=out_dtype)
+    ref_out, ref_lse = cp.cp_ring_forward_steps(q, k, v, P, layout, out_dtype=out_dtype)
     out, lse = torch.empty_like(ref_out), torch.empty_like(ref_lse)
     n = cp.cp_ring_workspace_size(S, H, D, out_dtype)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
@@ -125,7 +193,7 @@ def test_ring_overlapped_steps_equal_separate_steps(cp, layout, out_dtype):
         cp.cp_ring_step(q, k, v, P, layout, t, out, lse, ws if n else None)
     cp.cp_check_device_error()
     assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
-    again = cp.cp_ring_forward(q, k, v, P, layout, out_dtype=out_dtype)
+    again = cp.cp_ring_forward_steps(q, k, v, P, layout, out_dtype=out_dtype)
     assert torch.equal(again[0], ref_out) and torch.equal(again[1], ref_lse)
 
 
@@ -304,7 +372,7 @@ def test_ring_copy_mode_equals_in_place(cp, S, P, layout):
     """KV passed rank to rank through double buffers on a second stream gives
     the same bits as the in-place ring, and matches the oracle."""
     q, k, v = make_qkv(S, 8, 128, Hkv=4, dtype=torch.bfloat16, seed=S + P, device="cuda")
-    ref = cp.cp_ring_forward(q, k, v, P, layout, out_dtype=torch.bfloat16)
+    ref = ring_by_steps(cp, q, k, v, P, layout, out_dtype=torch.bfloat16)
     side = torch.cuda.Stream()
     out, lse = cp.cp_ring_forward_copy(q, k, v, P, layout, out_dtype=torch.bfloat16,
                                        copy_stream=side)
@@ -363,7 +431,7 @@ def test_ring_host_equals_device_ring(cp, layout, groups, Hkv, pinned, two_strea
     S, H, D, P = 1536, 8, 128, 4
     q, k, v = make_qkv(S, H, D, Hkv=Hkv, dtype=torch.bfloat16, seed=5)
     ref_out, ref_lse = cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), P, layout,
-                                          out_dtype=torch.bfloat16)
+                                     out_dtype=torch.bfloat16)
     if pinned:
         q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
     side = torch.cuda.Stream() if two_streams else None
@@ -417,7 +485,7 @@ def test_ring_host_back_to_back_calls(cp):
     cp.cp_check_device_error()
     for (q, k, v), (hout, hlse) in zip(ins, outs):
         ro, rl = cp.cp_ring_forward(q.to(dev), k.to(dev), v.to(dev), P, "zigzag",
-                                    out_dtype=torch.bfloat16)
+                               out_dtype=torch.bfloat16)
         assert torch.equal(hout, ro.cpu()) and torch.equal(hlse, rl.cpu())
 
 
@@ -458,24 +526,27 @@ def test_usp_stages_equal_forward(cp, layout):
 
 
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
-def test_ring_forward_in_cuda_graph(cp, layout):
-    """cp_ring_forward captured into a CUDA graph (its steps after the first
-    carry programmatic dependencies) replays to the eager result bit for bit;
-    replaying is how a caller removes the host cost of small rings."""
+@pytest.mark.parametrize("entry", ["cp_ring_forward", "cp_ring_forward_steps"])
+def test_ring_forward_in_cuda_graph(cp, layout, entry):
+    """The ring captured into a CUDA graph (one launch; or one per step, those
+    after the first carrying programmatic dependencies) replays to the eager
+    result bit for bit; replaying is how a caller removes the host cost of
+    small rings."""
     S, H, D, P = 4096, 32, 128, 4
+    fn = getattr(cp, entry)
     q, k, v = make_qkv(S, H, D, dtype=torch.bfloat16, seed=31, device="cuda")
     out = torch.empty(S, H, D, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(H, S, dtype=torch.float32, device="cuda")
     ws = torch.empty(cp.cp_ring_workspace_size(S, H, D, torch.bfloat16), dtype=torch.uint8,
                      device="cuda")
-    ref = cp.cp_ring_forward(q, k, v, P, layout, out_dtype=torch.bfloat16)
+    ref = fn(q, k, v, P, layout, out_dtype=torch.bfloat16)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        cp.cp_ring_forward(q, k, v, P, layout, out=out, lse=lse, workspace=ws, stream=s)
+        fn(q, k, v, P, layout, out=out, lse=lse, workspace=ws, stream=s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            cp.cp_ring_forward(q, k, v, P, layout, out=out, lse=lse, workspace=ws, stream=s)
+            fn(q, k, v, P, layout, out=out, lse=lse, workspace=ws, stream=s)
         out.zero_()
         lse.zero_()
         for _ in range(3):
@@ -494,7 +565,7 @@ def test_ring_host_ragged(cp, S, layout, out_dtype):
     H, D, P = 8, 128, 4
     q, k, v = make_qkv(S, H, D, Hkv=4, dtype=torch.bfloat16, seed=17)
     ref_out, ref_lse = cp.cp_ring_forward(q.cuda(), k.cuda(), v.cuda(), P, layout,
-                                          out_dtype=out_dtype)
+                                     out_dtype=out_dtype)
     hout, out_ok = guarded((S, H, D), out_dtype, pin=True)
     hlse, lse_ok = guarded((H, S), torch.float32, pin=True)
     cp.cp_ring_forward_host(*(t.pin_memory() for t in (q, k, v)), P, layout, hout=hout,

@@ -1,8 +1,8 @@
 """cp_ring_forward_noalloc: the ring forward for callers that may not allocate
 device memory (a plugin inside a host framework's fixed memory budget, or a
 latency-critical loop where cudaMalloc/cudaFree would synchronise the
-device).  Its fp32 accumulator is a fixed array inside the library instead of
-a caller workspace.
+device).  When the ring runs step by step its fp32 accumulator is a fixed
+array inside the library instead of a caller workspace.
 
 This file is collected last on purpose, so that a run stopping at the first
 failure has already run every other test.  It passes alone in a fresh
@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from context_causal_attention_attn_gb300.inputs import make_qkv
+from context_causal_attention_attn_gb300.inputs import make_qkv, sample_rows
 from gpu_common import ATOL_BF16_LSE, ATOL_BF16_OUT, ATOL_F32, compare, host
 
 
@@ -27,26 +27,44 @@ def cp():
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_version_twice(cp):
-    """Two calls in a row through the C ABI give the bits of cp_ring_forward
-    (which takes a caller workspace; both run the same launches), so they are
-    also within the suite's bf16 tolerances; the first call is also checked
-    against the oracle on every row."""
-    S, H, D, P = 4096, 32, 128, 4
+    """Two calls in a row through the C ABI on a ring that runs step by step
+    (the striped layout; its fp32 accumulator then lives in the library's
+    scratch array, S*H*D exactly the scratch's limit) agree with
+    cp_ring_forward (which takes a caller workspace) within the suite's bf16
+    tolerances -- bit for bit, as both run the same launches -- and the first
+    call also with the oracle on 512 seeded rows per head."""
+    S, H, D, P = 16384, 8, 128, 8
     q, k, v = make_qkv(S, H, D, dtype=torch.bfloat16, device="cuda", seed=3)
-    ref_out, ref_lse = cp.cp_ring_forward(q, k, v, P, "zigzag", out_dtype=torch.bfloat16)
+    assert not cp.ring_runs_fused(q, "striped")  # step by step: the scratch is used
+    ref_out, ref_lse = cp.cp_ring_forward(q, k, v, P, "striped", out_dtype=torch.bfloat16)
     cp.cp_check_device_error()
     for call in range(2):
         out = torch.full_like(ref_out, float("nan"))
         lse = torch.full_like(ref_lse, float("nan"))
-        cp.cp_ring_forward_noalloc(q, k, v, P, "zigzag", out=out, lse=lse)
+        cp.cp_ring_forward_noalloc(q, k, v, P, "striped", out=out, lse=lse)
         cp.cp_check_device_error()
         d_out = (out.float() - ref_out.float()).abs().max().item()
         d_lse = (lse - ref_lse).abs().max().item()
         assert d_out <= ATOL_BF16_OUT and d_lse <= ATOL_BF16_LSE, (d_out, d_lse)
         assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse), call
         if call == 0:
-            ro, rl = oracle.attention(host(q), host(k), host(v))
-            compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE)
+            rows = sample_rows(S, 512, seed=1, must=(0, S - 1))
+            ro, rl = oracle.attention_monolithic(host(q), host(k), host(v), rows=rows)
+            compare(out, lse, ro, rl, ATOL_BF16_OUT, ATOL_BF16_LSE, rows=rows)
+
+
+@pytest.mark.gpu
+def test_noalloc_one_launch_ring_uses_no_scratch(cp):
+    """A ring cp_ring_forward runs in one launch (bf16, zigzag) keeps no
+    accumulator: the call accepts sizes past the scratch's limit (S*H*D =
+    33,554,432 here) and equals cp_ring_forward."""
+    S, H, D, P = 8192, 32, 128, 4
+    q, k, v = make_qkv(S, H, D, dtype=torch.bfloat16, device="cuda", seed=4)
+    assert cp.ring_runs_fused(q, "zigzag")
+    ref_out, ref_lse = cp.cp_ring_forward(q, k, v, P, "zigzag", out_dtype=torch.bfloat16)
+    out, lse = cp.cp_ring_forward_noalloc(q, k, v, P, "zigzag", out_dtype=torch.bfloat16)
+    cp.cp_check_device_error()
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
 @pytest.mark.gpu
@@ -67,8 +85,8 @@ def test_noalloc_fp32_output_uses_no_scratch(cp):
 
 @pytest.mark.gpu
 def test_noalloc_rejects_sizes_beyond_the_scratch(cp):
-    S, H, D, P = 8192, 32, 128, 8  # needs 128 MiB of accumulator
+    S, H, D, P = 16384, 16, 128, 8  # a step-by-step ring needing 128 MiB of accumulator
     q = torch.empty(S, H, D, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(cp.CpError) as e:
-        cp.cp_ring_forward_noalloc(q, q, q, P, "zigzag", out_dtype=torch.bfloat16)
+        cp.cp_ring_forward_noalloc(q, q, q, P, "striped", out_dtype=torch.bfloat16)
     assert "scratch" in str(e.value)
