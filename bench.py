@@ -244,24 +244,44 @@ def near_gpu(local):
             os.sched_setaffinity(0, old)
 
 
-def link_gbs(dev_t, host_t, stream, reps=3):
+def link_gbs(dev_t, host_t, stream, samples=5):
     """Host-to-device and device-to-host GB/s of plain copies between a
-    page-locked host tensor and a device tensor of the same size, timed
-    with CUDA events on ``stream``."""
+    page-locked host tensor and a device tensor of the same size, each copy
+    timed alone with CUDA events on ``stream``.  Returns (median H2D, median
+    D2H, bytes, {"h2d": [min, max], "d2h": [min, max]}): the host link of a
+    shared machine can slow down for seconds at a time, which the spread
+    shows."""
     import torch
     nbytes = dev_t.numel() * dev_t.element_size()
-    res = []
+    med, spread = [], {}
     for h2d in (True, False):
         dst, src = (dev_t, host_t) if h2d else (host_t, dev_t)
         dst.copy_(src, non_blocking=True)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
+        rates = []
+        for _ in range(samples):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
             dst.copy_(src, non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        res.append(round(reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9, 1))
-    return res[0], res[1], nbytes
+            e1.record(stream)
+            e1.synchronize()
+            rates.append(nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        med.append(round(statistics.median(rates), 1))
+        spread["h2d" if h2d else "d2h"] = [round(min(rates), 1), round(max(rates), 1)]
+    return med[0], med[1], nbytes, spread
+
+
+def timed_calls(fn, n, stream):
+    """Run fn n times back to back with an event between calls; returns
+    (total ms, [ms per call])."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
+        fn()
+        evs[i + 1].record(stream)
+    evs[n].synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    return evs[0].elapsed_time(evs[n]), per
 
 
 def timed_steps(step, K, min_timed_s, stream):
@@ -484,7 +504,7 @@ def run_gpu(args, wl, rank, world, local):
         hlse = torch.empty(H, S, dtype=torch.float32, pin_memory=True)
     for h_, d_ in ((hq, q), (hk, k), (hv, v)):
         h_.copy_(d_)
-    h2d_gbs, d2h_gbs, link_bytes = link_gbs(q, hq, stream)
+    h2d_gbs, d2h_gbs, link_bytes, link_spread = link_gbs(q, hq, stream)
     q.copy_(hq)
     K_e2e = max(1, min(K, 3))
     host_api = wl["kind"] in ("ring", "ring_steps", "ulysses", "usp")
@@ -543,14 +563,9 @@ def run_gpu(args, wl, rank, world, local):
     e2e_step()
     torch.cuda.synchronize(dev)
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K_e2e):
-        e2e_step()
-    e1.record(stream)
+    e2e_ms, e2e_calls = timed_calls(e2e_step, K_e2e, stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e_ms = reduce_max(e2e_ms, world)
     cp.cp_check_device_error(stream)
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = out.numel() * 2 + lse.numel() * 4
@@ -586,8 +601,9 @@ def run_gpu(args, wl, rank, world, local):
                 "api": (host_fn + f" (pinned host buffers, {groups} head groups, copies on a "
                         "second stream)") if host_api else
                        "pinned host copies + device entry point on one stream",
-                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
-                "link_note": (f"plain pinned copies of q ({link_bytes >> 20} MiB) each way; "
+                "ms_per_call": [round(x, 3) for x in e2e_calls],
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "link_gbs_min_max": link_spread,
+                "link_note": (f"median of 5 plain pinned copies of q ({link_bytes >> 20} MiB) each way; "
                               f"host buffers on NUMA node {numa_node}" if numa_node is not None
                               else f"plain pinned copies of q ({link_bytes >> 20} MiB) each "
                               "way; the GPU's NUMA node is not reported, host buffers where "
@@ -765,7 +781,7 @@ def run_bwd(args, wl, rank, world, local):
         host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     for h_, d_ in zip(host_in, src):
         h_.copy_(d_)
-    h2d_gbs, d2h_gbs, link_bytes = link_gbs(dq, host_out[0], stream)
+    h2d_gbs, d2h_gbs, link_bytes, link_spread = link_gbs(dq, host_out[0], stream)
     K_e2e = max(1, min(K, 3))
     host_api = not train
     if host_api:
@@ -797,14 +813,9 @@ def run_bwd(args, wl, rank, world, local):
     e2e_step()
     torch.cuda.synchronize(dev)
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K_e2e):
-        e2e_step()
-    e1.record(stream)
+    e2e_ms, e2e_calls = timed_calls(e2e_step, K_e2e, stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e_ms = reduce_max(e2e_ms, world)
     cp.cp_check_device_error(stream)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
@@ -854,8 +865,9 @@ def run_bwd(args, wl, rank, world, local):
                 "api": (f"cp_ring_backward_host (pinned host buffers, {groups} head groups, "
                         "copies on a second stream)") if host_api else
                        "pinned host copies + device entry points on one stream",
-                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
-                "link_note": (f"plain pinned copies of {link_bytes >> 20} MiB each way; host "
+                "ms_per_call": [round(x, 3) for x in e2e_calls],
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "link_gbs_min_max": link_spread,
+                "link_note": (f"median of 5 plain pinned copies of {link_bytes >> 20} MiB each way; host "
                               f"buffers on NUMA node {numa_node}" if numa_node is not None else
                               f"plain pinned copies of {link_bytes >> 20} MiB each way; the "
                               "GPU's NUMA node is not reported")},
@@ -944,7 +956,7 @@ def run_hbm(args, wl, rank, world, local):
         hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in result_t]
     for h_, d_ in zip(hin, inputs):
         h_.copy_(d_)
-    h2d_gbs, d2h_gbs, _ = link_gbs(inputs[0], hin[0], stream)
+    h2d_gbs, d2h_gbs, _, link_spread = link_gbs(inputs[0], hin[0], stream)
     inputs[0].copy_(hin[0])
     K_e2e = max(1, min(K, 3))
     f0 = torch.cuda.Event(enable_timing=True)
@@ -978,7 +990,8 @@ def run_hbm(args, wl, rank, world, local):
         "e2e": {"value": round(world * algo * K_e2e / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in inputs),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in result_t),
-                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "host_numa_node": numa_node},
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "link_gbs_min_max": link_spread,
+                "host_numa_node": numa_node},
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": round(gbs / world, 1),
                      "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                      "frac": round(gbs / world / float(peaks["hbm_gbs"]), 4), "traffic": None,
