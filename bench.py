@@ -724,8 +724,13 @@ def run_bwd(args, wl, rank, world, local):
     # ring where it runs fused, else one per step)
     fwd_launches = [("fwd", -1)] if cp.ring_runs_fused(q, layout) else [
         ("fwd", t) for t in range(P)]
+    # the backward: cp_ring_backward's schedule (for bf16 contiguous / zigzag
+    # one dK/dV and one dQ launch over every step, else one of each per step)
+    fused_bwd = cp.ring_runs_fused(q, layout)
+    bstep = cp.cp_ring_backward_fused_step if fused_bwd else cp.cp_ring_backward_step
+    nbl = 2 if fused_bwd else 2 * P
     launches = (fwd_launches if train else []) + [("delta", -1)] + [
-        ("dkdv" if l % 2 == 0 else "dq", l) for l in range(2 * P)]
+        ("dkdv" if l % 2 == 0 else "dq", l) for l in range(nbl)]
 
     def launch(kind, l, tensors=(q, k, v, do)):
         q_, k_, v_, do_ = tensors
@@ -735,8 +740,7 @@ def run_bwd(args, wl, rank, world, local):
         elif kind == "fwd":
             cp.cp_ring_step(q_, k_, v_, P, layout, l, out, lse, fws, stream=stream)
         else:
-            cp.cp_ring_backward_step(q_, k_, v_, out, do_, lse, P, layout, l, dq, dk, dv, bws,
-                                     stream=stream)
+            bstep(q_, k_, v_, out, do_, lse, P, layout, l, dq, dk, dv, bws, stream=stream)
 
     def step(tensors=(q, k, v, do)):
         if train:
@@ -850,6 +854,9 @@ def run_bwd(args, wl, rank, world, local):
                    "layout": layout, "in_dtype": "bf16", "grad_dtype": "bf16",
                    "accumulate": "fp32", "causal": True,
                    "pass": "forward + backward" if train else "backward",
+                   "ring_impl": ("one dK/dV and one dQ launch over all steps (each "
+                                 "stationary tile keeps its gradient on chip)" if fused_bwd else
+                                 "one dK/dV and one dQ launch per step, accumulating in fp32"),
                    "l2": f"inputs larger than L2 ({h2d >> 20} MiB per rank)",
                    "flops_per_step": flops,
                    "flops_count": ("3.5x" if train else "2.5x") + " causal forward FLOPs",

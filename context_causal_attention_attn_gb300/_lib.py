@@ -96,6 +96,8 @@ def lib():
                                    vp, vp, vp, i32, vp, vp]),
         "cp_ring_backward_step": (i32, [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32,
                                         i32, i32, vp, vp, vp, i32, vp, vp]),
+        "cp_ring_backward_fused_step": (i32, [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                              i32, i32, i32, vp, vp, vp, i32, vp, vp]),
         "cp_check_device_error": (i32, [vp]),
         "cp_selftest_wait_timeout": (i32, [i32, vp]),
         "cp_last_error": (ctypes.c_char_p, []),
@@ -681,11 +683,25 @@ def cp_ring_backward_host(hq, hk, hv, hout, hdout, hlse, P, layout="zigzag", gra
 
 def cp_ring_backward_step(q, k, v, out, dout, lse, P, layout, launch, dq, dk, dv, workspace,
                           stream=None):
-    """One launch of cp_ring_backward: -1 delta, 2t dK/dV of step t, 2t+1 dQ of step t."""
+    """One launch of the per-step ring backward: -1 delta, 2t dK/dV of step t,
+    2t+1 dQ of step t."""
     S, H, D = q.shape
     Hkv = k.shape[1]
     _dev(q, k, v, out, dout, lse, dq, dk, dv, workspace)
     _check(lib().cp_ring_backward_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _dt(q), S, H, Hkv, D,
+        int(P), _layout(layout), int(launch), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq),
+        _ptr(workspace), _stream(stream)))
+
+
+def cp_ring_backward_fused_step(q, k, v, out, dout, lse, P, layout, launch, dq, dk, dv,
+                                workspace, stream=None):
+    """One launch of the two-launch ring backward (bf16, contiguous or zigzag):
+    -1 delta, 0 dK/dV over every step, 1 dQ over every step."""
+    S, H, D = q.shape
+    Hkv = k.shape[1]
+    _dev(q, k, v, out, dout, lse, dq, dk, dv, workspace)
+    _check(lib().cp_ring_backward_fused_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _dt(q), S, H, Hkv, D,
         int(P), _layout(layout), int(launch), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq),
         _ptr(workspace), _stream(stream)))

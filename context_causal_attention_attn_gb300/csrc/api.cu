@@ -552,6 +552,7 @@ struct BwdTask {
   bool dkdv;
   std::vector<BwdItem> items;
   std::vector<int> chunk;
+  int64_t ring_C = 0, ring_S = 0;  // chunk geometry of chunk-list items
 };
 
 struct BwdArgs {
@@ -592,6 +593,8 @@ int run_bwd_task(const BwdArgs& a, const BwdTask& t, const CUtensorMap maps[4], 
   p.lse = a.lse;
   p.delta = a.delta;
   p.ld = a.ld;
+  p.ring_C = t.ring_C;
+  p.ring_S = t.ring_S;
   if (t.dkdv) {
     p.acc0 = a.acc_v;
     p.acc1 = a.acc_k;
@@ -742,6 +745,84 @@ std::vector<BwdTask> ring_bwd_tasks(int64_t S, int P, cp_layout layout) {
     tasks.push_back(tq);
   }
   return tasks;
+}
+
+// The ring's backward in two launches (bf16, contiguous or zigzag): the dK/dV
+// kernel runs one item per KV chunk, streaming the query chunks that see it
+// in the order the ring's steps bring them (at step t the chunk sits with
+// rank owner + t, whose own query chunks not earlier than it are evaluated);
+// the dQ kernel one item per (rank, own query chunk), streaming the KV chunks
+// the rank holds at steps 0 .. P-1 not later than it -- the forward's walk.
+// Each stationary tile keeps its gradient in TMEM across all steps and
+// writes it once.
+std::vector<BwdTask> ring_bwd_fused_tasks(int64_t S, int P, cp_layout layout) {
+  const int64_t nchunks = layout == CP_ZIGZAG ? 2 * P : P;
+  const int64_t C = (S + nchunks - 1) / nchunks;
+  auto rows = [&](int c) -> int32_t {
+    return static_cast<int32_t>(std::max<int64_t>(0, std::min<int64_t>(S, (c + 1) * C) - c * C));
+  };
+  auto seg = [&](int c) { return BwdSeg{c * C, c * C, rows(c), 0}; };
+  auto owner = [&](int c) { return layout == CP_ZIGZAG && c >= P ? static_cast<int>(2 * P - 1 - c) : c; };
+  BwdTask tk{true, {}, {}, C, S}, tq{false, {}, {}, C, S};
+  std::vector<int64_t> wk, wq;  // streamed rows, for the longest-first order
+  for (int kc = 0; kc < nchunks; ++kc) {
+    if (rows(kc) == 0) continue;
+    BwdItem it{};
+    it.stat = seg(kc);
+    int64_t w = 0;
+    for (int t = 0; t < P; ++t) {
+      int qcs[2];
+      const int nq = rank_chunks(P, layout, (owner(kc) + t) % P, qcs);
+      if (nq == 2 && qcs[0] > qcs[1]) std::swap(qcs[0], qcs[1]);
+      for (int a = 0; a < nq; ++a)
+        if (qcs[a] >= kc && rows(qcs[a]) > 0) {
+          it.chunk[it.nchunk++] = static_cast<uint8_t>(qcs[a]);
+          w += rows(qcs[a]);
+        }
+    }
+    if (it.nchunk == 0) continue;
+    tk.items.push_back(it);
+    tk.chunk.push_back(kc);
+    wk.push_back(w);
+  }
+  for (int r = 0; r < P; ++r) {
+    int qcs[2];
+    const int nq = rank_chunks(P, layout, r, qcs);
+    for (int a = 0; a < nq; ++a) {
+      const int qc = qcs[a];
+      if (rows(qc) == 0) continue;
+      BwdItem it{};
+      it.stat = seg(qc);
+      int64_t w = 0;
+      for (int t = 0; t < P; ++t) {
+        int kcs[2];
+        const int nk = rank_chunks(P, layout, ((r - t) % P + P) % P, kcs);
+        for (int b = 0; b < nk; ++b)
+          if (kcs[b] <= qc && rows(kcs[b]) > 0) {
+            it.chunk[it.nchunk++] = static_cast<uint8_t>(kcs[b]);
+            w += rows(kcs[b]);
+          }
+      }
+      tq.items.push_back(it);
+      tq.chunk.push_back(qc);
+      wq.push_back(w);
+    }
+  }
+  // longest items first (the grid is scheduled roughly in order)
+  auto sort_task = [](BwdTask& t, const std::vector<int64_t>& w) {
+    std::vector<size_t> o(t.items.size());
+    for (size_t i = 0; i < o.size(); ++i) o[i] = i;
+    std::stable_sort(o.begin(), o.end(), [&](size_t a, size_t b) { return w[a] > w[b]; });
+    BwdTask s{t.dkdv, {}, {}, t.ring_C, t.ring_S};
+    for (size_t i : o) {
+      s.items.push_back(t.items[i]);
+      s.chunk.push_back(t.chunk[i]);
+    }
+    t = s;
+  };
+  sort_task(tk, wk);
+  sort_task(tq, wq);
+  return {tk, tq};
 }
 
 int check_bwd_common(cp_dtype in_dt, int H, int Hkv, int D, cp_dtype grad_dt) {
@@ -1600,16 +1681,24 @@ int64_t cp_ring_backward_workspace_size(int64_t S, int H, int Hkv, int D, cp_dty
   return b;
 }
 
-int cp_ring_backward_step(const void* q, const void* k, const void* v, const void* out,
-                          const void* dout, const float* lse, cp_dtype in_dt, int64_t S, int H,
-                          int Hkv, int D, int P, cp_layout layout, int launch, void* dq,
-                          void* dk, void* dv, cp_dtype grad_dt, void* workspace,
-                          cp_stream_t stream) {
+// Launch `launch` of the ring backward's per-step schedule (fused = false:
+// -1 delta, 2t dK/dV of step t, 2t + 1 dQ of step t) or of its two-launch
+// schedule (fused = true: -1 delta, 0 dK/dV, 1 dQ).
+static int ring_backward_launch(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse, cp_dtype in_dt, int64_t S,
+                                int H, int Hkv, int D, int P, cp_layout layout, int launch,
+                                void* dq, void* dk, void* dv, cp_dtype grad_dt, void* workspace,
+                                cp_stream_t stream, bool fused) {
   int rc = check_bwd_common(in_dt, H, Hkv, D, grad_dt);
   if (rc != CP_OK) return rc;
   if ((rc = check_ring(in_dt, S, H, Hkv, D, P, layout, grad_dt)) != CP_OK) return rc;
-  if (launch < -1 || launch >= 2 * P)
-    return fail(CP_ERR_ARG, "launch=%d outside [-1,%d)", launch, 2 * P);
+  if (fused && !ring_runs_fused(in_dt, layout))
+    return fail(in_dt != CP_BF16 ? CP_ERR_DTYPE : CP_ERR_ARG,
+                "the two-launch ring backward needs bf16 inputs and the contiguous or zigzag "
+                "layout");
+  const int nl = fused ? 2 : 2 * P;
+  if (launch < -1 || launch >= nl)
+    return fail(CP_ERR_ARG, "launch=%d outside [-1,%d)", launch, nl);
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace)
     return fail(CP_ERR_ARG, "null pointer argument");
   for (const void* x : {q, k, v, out, dout, static_cast<const void*>(dq),
@@ -1637,18 +1726,41 @@ int cp_ring_backward_step(const void* q, const void* k, const void* v, const voi
   BwdArgs a{q, k, v, dout, S, S, H, Hkv, striped ? P : 1, 1, in_dt, D,
             1.0f / std::sqrt(static_cast<float>(D)), lse, delta, S, grad_dt, dq, dk, dv,
             acc_q, acc_k, acc_v};
-  std::vector<BwdTask> tasks = ring_bwd_tasks(S, P, layout);
+  std::vector<BwdTask> tasks =
+      fused ? ring_bwd_fused_tasks(S, P, layout) : ring_bwd_tasks(S, P, layout);
   rc = run_bwd_tasks(a, tasks, s, launch);
   return rc == CP_OK ? ok() : rc;
+}
+
+int cp_ring_backward_step(const void* q, const void* k, const void* v, const void* out,
+                          const void* dout, const float* lse, cp_dtype in_dt, int64_t S, int H,
+                          int Hkv, int D, int P, cp_layout layout, int launch, void* dq,
+                          void* dk, void* dv, cp_dtype grad_dt, void* workspace,
+                          cp_stream_t stream) {
+  return ring_backward_launch(q, k, v, out, dout, lse, in_dt, S, H, Hkv, D, P, layout, launch,
+                              dq, dk, dv, grad_dt, workspace, stream, false);
+}
+
+int cp_ring_backward_fused_step(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse, cp_dtype in_dt, int64_t S,
+                                int H, int Hkv, int D, int P, cp_layout layout, int launch,
+                                void* dq, void* dk, void* dv, cp_dtype grad_dt, void* workspace,
+                                cp_stream_t stream) {
+  return ring_backward_launch(q, k, v, out, dout, lse, in_dt, S, H, Hkv, D, P, layout, launch,
+                              dq, dk, dv, grad_dt, workspace, stream, true);
 }
 
 int cp_ring_backward(const void* q, const void* k, const void* v, const void* out,
                      const void* dout, const float* lse, cp_dtype in_dt, int64_t S, int H,
                      int Hkv, int D, int P, cp_layout layout, void* dq, void* dk, void* dv,
                      cp_dtype grad_dt, void* workspace, cp_stream_t stream) {
-  for (int l = -1; l < 2 * P; ++l) {
-    const int rc = cp_ring_backward_step(q, k, v, out, dout, lse, in_dt, S, H, Hkv, D, P, layout,
-                                         l, dq, dk, dv, grad_dt, workspace, stream);
+  // the tensor-core path runs the ring in two launches (every step inside
+  // each), the rest one dK/dV and one dQ launch per step
+  const bool fused = ring_runs_fused(in_dt, layout);
+  const int nl = fused ? 2 : 2 * P;
+  for (int l = -1; l < nl; ++l) {
+    const int rc = ring_backward_launch(q, k, v, out, dout, lse, in_dt, S, H, Hkv, D, P, layout,
+                                        l, dq, dk, dv, grad_dt, workspace, stream, fused);
     if (rc != CP_OK) return rc;
   }
   return ok();

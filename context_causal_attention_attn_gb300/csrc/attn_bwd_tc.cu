@@ -110,66 +110,126 @@ static_assert(Smem<false>::USED <= SMEM_LIMIT, "dQ shared memory");
 
 __device__ __forceinline__ int bw_tiles(int len) { return (len + bw::BN - 1) / bw::BN; }
 
-// Streamed tiles of an item, in order.  kDKDV = false: key tiles of the
-// streamed segments visible to a query at qp_last (a prefix).  kDKDV = true:
-// query tiles with a query at or after the stationary key at kp_first (a
-// suffix of each segment), counted per query head of the group.
+// Streamed segment s of an item: str[s], or for a chunk-list item (a whole
+// ring in one launch) sequence chunk chunk[s].
+__device__ __forceinline__ int bw_nstr(const BwdItem& it) {
+  return it.nchunk > 0 ? it.nchunk : it.nstr;
+}
+__device__ __forceinline__ void bw_str(const BwdItem& it, const BwdParams& p, int s,
+                                       int64_t& row, int64_t& pos, int& len, int& stripe) {
+  if (it.nchunk > 0) {
+    const int64_t c0 = static_cast<int64_t>(it.chunk[s]) * p.ring_C;
+    row = c0;
+    pos = c0;
+    len = static_cast<int>(min(p.ring_S - c0, p.ring_C));
+    stripe = 0;
+  } else {
+    row = it.str[s].row;
+    pos = it.str[s].pos;
+    len = it.str[s].len;
+    stripe = it.str[s].stripe;
+  }
+}
+
+// Streamed tiles [t0, t1) of a segment the stationary tile uses.  kDKDV =
+// false: key tiles visible to a query at lim_pos (a prefix).  kDKDV = true:
+// query tiles with a query at or after the stationary key at lim_pos (a
+// suffix).
 template <bool kDKDV>
-__device__ __forceinline__ int bw_count(const BwdItem& it, int64_t lim_pos, bool causal) {
+__device__ __forceinline__ void bw_vis(int64_t pos, int len, int64_t lim_pos, bool causal,
+                                       int& t0, int& t1) {
+  const int T = bw_tiles(len);
+  t0 = 0;
+  t1 = T;
+  if (!causal) return;
+  if (!kDKDV) {
+    if (lim_pos < pos) {
+      t1 = 0;
+      return;
+    }
+    const int64_t v = (lim_pos - pos) / bw::BN + 1;
+    if (v < T) t1 = static_cast<int>(v);
+  } else {
+    if (pos + len - 1 < lim_pos) {  // every query before the keys
+      t1 = 0;
+      return;
+    }
+    t0 = lim_pos > pos ? static_cast<int>((lim_pos - pos) / bw::BN) : 0;
+  }
+}
+
+// Streamed tiles of an item per head (the dK/dV kernel runs them once per
+// query head of its group).
+template <bool kDKDV>
+__device__ __forceinline__ int bw_count(const BwdItem& it, const BwdParams& p, int64_t lim_pos,
+                                        bool causal) {
   int n = 0;
-  for (int s = 0; s < it.nstr; ++s) {
-    const BwdSeg& g = it.str[s];
-    const int T = bw_tiles(g.len);
-    if (!causal) {
-      n += T;
-      continue;
-    }
-    if (!kDKDV) {
-      if (lim_pos < g.pos) break;
-      const int64_t v = (lim_pos - g.pos) / bw::BN + 1;
-      if (v < T) {
-        n += static_cast<int>(v);
-        break;
-      }
-      n += T;
-    } else {
-      if (g.pos + g.len - 1 < lim_pos) continue;  // every query before the keys
-      const int tmin = lim_pos > g.pos ? static_cast<int>((lim_pos - g.pos) / bw::BN) : 0;
-      n += T - tmin;
-    }
+  const int ns = bw_nstr(it);
+  for (int s = 0; s < ns; ++s) {
+    int64_t row, pos;
+    int len, stripe, t0, t1;
+    bw_str(it, p, s, row, pos, len, stripe);
+    bw_vis<kDKDV>(pos, len, lim_pos, causal, t0, t1);
+    n += t1 - t0;
   }
   return n;
 }
 
-// Tile k (0-based, within one head) of the streamed segments -> first row,
-// first position, valid rows and stripe.
+// Walks the streamed tiles of an item in order -- segment by segment, and
+// for the dK/dV kernel head by head of the query group -- keeping only its
+// position (a tile's rows are re-derived from the item when asked for).
 template <bool kDKDV>
-__device__ __forceinline__ void bw_tile(const BwdItem& it, int k, int64_t lim_pos, bool causal,
-                                        int64_t& row, int64_t& pos, int& n, int& stripe) {
-  for (int s = 0; s < it.nstr; ++s) {
-    const BwdSeg& g = it.str[s];
-    const int T = bw_tiles(g.len);
-    int tmin = 0;
-    if (kDKDV && causal) {
-      if (g.pos + g.len - 1 < lim_pos) continue;
-      tmin = lim_pos > g.pos ? static_cast<int>((lim_pos - g.pos) / bw::BN) : 0;
+struct BwCursor {
+  int s, t, tend;  // segment, tile within it, end of its used tiles
+  int k, g;        // tile within the head, query head within the group
+  __device__ __forceinline__ void seek(const BwdItem& it, const BwdParams& p, int64_t lim,
+                                       bool causal) {
+    const int ns = bw_nstr(it);
+    for (; s < ns; ++s) {
+      int64_t row, pos;
+      int len, stripe, t0;
+      bw_str(it, p, s, row, pos, len, stripe);
+      bw_vis<kDKDV>(pos, len, lim, causal, t0, tend);
+      if (t0 < tend) {
+        t = t0;
+        return;
+      }
     }
-    const int cnt = T - tmin;
-    if (k < cnt) {
-      const int t = tmin + k;
-      row = g.row + static_cast<int64_t>(t) * bw::BN;
-      pos = g.pos + static_cast<int64_t>(t) * bw::BN;
-      n = min(bw::BN, g.len - t * bw::BN);
-      stripe = g.stripe;
+  }
+  __device__ __forceinline__ void init(const BwdItem& it, const BwdParams& p, int64_t lim,
+                                       bool causal) {
+    s = 0;
+    t = 0;
+    tend = 0;
+    k = 0;
+    g = 0;
+    seek(it, p, lim, causal);
+  }
+  // to the next tile; nper = tiles per head
+  __device__ __forceinline__ void next(const BwdItem& it, const BwdParams& p, int64_t lim,
+                                       bool causal, int nper) {
+    if (++k == nper) {  // the next query head of the group starts over
+      k = 0;
+      ++g;
+      s = 0;
+      seek(it, p, lim, causal);
       return;
     }
-    k -= cnt;
+    if (++t >= tend) {
+      ++s;
+      seek(it, p, lim, causal);
+    }
   }
-  row = 0;
-  pos = 0;
-  n = 0;
-  stripe = 0;
-}
+  // the current tile: first row, first position, valid rows, stripe
+  __device__ __forceinline__ void tile(const BwdItem& it, const BwdParams& p, int64_t& row,
+                                       int64_t& pos, int& n, int& stripe) const {
+    int len;
+    bw_str(it, p, s, row, pos, len, stripe);
+    row += static_cast<int64_t>(t) * bw::BN;
+    pos += static_cast<int64_t>(t) * bw::BN;
+    n = min(bw::BN, len - t * bw::BN);
+  }
+};
 
 __device__ __forceinline__ void bw_timeout(int* dev_err, volatile int* abort_flag) {
   *abort_flag = 1;
@@ -221,7 +281,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   const int nstat = min(bw::BM, it.stat.len - stile * bw::BM);
   // visibility limit: last query position (dQ) / first key position (dK/dV)
   const int64_t lim = kDKDV ? spos0 : spos0 + nstat - 1;
-  const int nper = bw_count<kDKDV>(it, lim, causal);
+  const int nper = bw_count<kDKDV>(it, p, lim, causal);
   const int nstr = kDKDV ? nper * grp : nper;
   const int kvh = kDKDV ? shead : shead / grp;
   const int64_t stride = kStriped ? p.stride : 1;
@@ -262,11 +322,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   constexpr int NA = bw::Rings<kDKDV>::NA, NB = bw::Rings<kDKDV>::NB;
   auto slot_of = [](int j, int w) { return w == 0 ? j % NA : NA + j % NB; };
   auto use_of = [](int j, int w) { return w == 0 ? j / NA : j / NB; };
-  // streamed tile j -> (row, pos, rows, stripe, query head)
-  auto str_tile = [&](int j, int64_t& row, int64_t& pos, int& n, int& stripe, int& qh) {
-    const int g = kDKDV ? j / max(nper, 1) : 0;
-    bw_tile<kDKDV>(it, kDKDV ? j - g * nper : j, lim, causal, row, pos, n, stripe);
-    qh = kDKDV ? shead * grp + g : shead;
+  // the cursor's tile -> (row, pos, rows, stripe, query head), then advance
+  auto str_tile = [&](BwCursor<kDKDV>& c, int64_t& row, int64_t& pos, int& n, int& stripe,
+                      int& qh) {
+    c.tile(it, p, row, pos, n, stripe);
+    qh = kDKDV ? shead * grp + c.g : shead;
+    c.next(it, p, lim, causal, nper);
   };
   auto load = [&](uint32_t dst, const CUtensorMap* tm, uint32_t b, int c0, int head, int stripe,
                   int64_t row, uint64_t pol) {
@@ -294,10 +355,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
           load(sStat + w * bw::TILE_BYTES + hh * bw::BOX_BYTES, w == 0 ? st0 : st1,
                bar(bw::BAR_STAT), hh * 64, sh, it.stat.stripe, srow0, pol_stat);
       int issued = 0;  // tiles whose loads were issued
+      BwCursor<kDKDV> pc;
+      pc.init(it, p, lim, causal);
       for (int j = 0; j < nstr; ++j) {
         int64_t row, pos;
         int n, stripe, qh;
-        str_tile(j, row, pos, n, stripe, qh);
+        str_tile(pc, row, pos, n, stripe, qh);
         bool ok = true;
         for (int w = 0; w < 2; ++w) {
           const int st = slot_of(j, w);
@@ -469,19 +532,24 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     // delta of column t - 128), loaded one tile ahead
     const int ccol = etid & (bw::BN - 1);
     const bool is_l = etid < bw::BN;
-    auto col_load = [&](int j) -> float {
+    // cursors of the tile loop and of the column loads (one tile ahead)
+    BwCursor<kDKDV> cc, lc;
+    cc.init(it, p, lim, causal);
+    lc = cc;
+    // the next tile's column value; called for tiles 0, 1, ... in order
+    auto col_load = [&]() -> float {
       int64_t trow, tpos;
       int tn, tstripe, qh;
-      str_tile(j, trow, tpos, tn, tstripe, qh);
+      str_tile(lc, trow, tpos, tn, tstripe, qh);
       if (ccol >= tn) return is_l ? CUDART_INF_F : 0.f;
       const int64_t tok = tstripe + stride * (trow + ccol);
       return (is_l ? p.lse : p.delta)[static_cast<int64_t>(qh) * p.ld + tok];
     };
-    float col_next = (kDKDV && nstr > 0) ? col_load(0) : 0.f;
+    float col_next = (kDKDV && nstr > 0) ? col_load() : 0.f;
     for (int j = 0; j < nstr; ++j) {
       int64_t trow, tpos;
       int tn, tstripe, qh;
-      str_tile(j, trow, tpos, tn, tstripe, qh);
+      str_tile(cc, trow, tpos, tn, tstripe, qh);
       float* cnl = cols + (j & 1) * 2 * bw::BN;  // dK/dV: per-column -LSE (log2)
       float* cdl = cnl + bw::BN;                 //        and delta
       if (kDKDV) {
@@ -491,7 +559,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         (is_l ? cnl : cdl)[ccol] =
             is_l ? ((x == -CUDART_INF_F || x == CUDART_INF_F) ? -CUDART_INF_F : -x * LOG2E) : x;
         named_bar_sync(1, bw::EW_THREADS);
-        if (j + 1 < nstr) col_next = col_load(j + 1);
+        if (j + 1 < nstr) col_next = col_load();
       }
       // visibility: key pos <= query pos, streamed index < tn; the visible
       // columns of this row are [c_lo, c_hi)

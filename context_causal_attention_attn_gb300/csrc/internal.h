@@ -138,6 +138,12 @@ struct BwdItem {
   BwdSeg str[kMaxSegs];
   int32_t nstr;
   int32_t flags;
+  // A whole ring in one launch: when nchunk > 0 the streamed segments are
+  // the sequence chunks chunk[0..nchunk) in the order the ring's steps reach
+  // them (chunk c = rows [c C, min(S, (c+1) C)) with C = BwdParams::ring_C,
+  // S = BwdParams::ring_S), and str / nstr are unused.
+  int32_t nchunk;
+  uint8_t chunk[kMaxRingChunks];
 };
 
 struct BwdParams {
@@ -156,6 +162,7 @@ struct BwdParams {
   int nitems;
   int cta_start[kMaxItems + 1];
   BwdItem items[kMaxItems];
+  int64_t ring_C, ring_S;  // chunk rows and sequence length of chunk-list items
 };
 
 }  // namespace cpattn

@@ -463,9 +463,11 @@ int cp_attn_block_backward(const void* q, const void* k, const void* v, const vo
  * same ring schedule: at step t virtual rank r evaluates the forward's
  * (query chunk, held KV chunk) pairs; dQ of its chunks accumulates in place,
  * dK / dV accumulate on the held chunk (in the ring they travel with it back
- * to their owner).  One launch of the dQ kernel and one of the dK/dV kernel
- * per step cover all ranks; the blocks use the whole-row lse, so the result
- * equals the gradients of monolithic causal attention up to rounding.
+ * to their owner).  For bf16 inputs in the contiguous or zigzag layout one
+ * dK/dV launch and one dQ launch cover every step (cp_ring_backward_fused_step),
+ * otherwise one of each per step covers all ranks (cp_ring_backward_step);
+ * the blocks use the whole-row lse, so the result equals the gradients of
+ * monolithic causal attention up to rounding.
  *
  *   q, out, dout [S,H,D], k, v [S,Hkv,D] in natural order; lse [H,S]
  *   the forward's; layouts and (S, P) conditions as cp_ring_forward.
@@ -476,19 +478,37 @@ int cp_attn_block_backward(const void* q, const void* k, const void* v, const vo
 int64_t cp_ring_backward_workspace_size(int64_t S, int H, int Hkv, int D, cp_dtype grad_dt);
 
 /*
- * cp_ring_backward_step - one launch of cp_ring_backward's schedule, for
- * callers that interleave their own work between launches (in a real ring:
- * sending a chunk's dK / dV on after the step that finished it) and for
- * timing.  launch = -1: the delta preprocessing; launch = 2t: the dK/dV
- * kernel of ring step t; launch = 2t + 1: the dQ kernel of step t
- * (0 <= t < P).  Running launch -1, 0, 1, ..., 2P-1 in order on one stream
- * is cp_ring_backward.  Arguments as cp_ring_backward.
+ * cp_ring_backward_step - one launch of the ring backward's per-step
+ * schedule, for callers that interleave their own work between launches
+ * (in a real ring: sending a chunk's dK / dV on after the step that
+ * finished it) and for timing.  launch = -1: the delta preprocessing;
+ * launch = 2t: the dK/dV kernel of ring step t, accumulating into the fp32
+ * gradient buffers; launch = 2t + 1: the dQ kernel of step t (0 <= t < P).
+ * Running launch -1, 0, 1, ..., 2P-1 in order on one stream is the ring
+ * backward step by step -- what cp_ring_backward runs for fp32 inputs and
+ * the striped layout.  Arguments as cp_ring_backward.
+ *
+ * cp_ring_backward_fused_step - one launch of the two-launch schedule that
+ * cp_ring_backward runs for bf16 inputs in the contiguous or zigzag layout
+ * (other inputs return CP_ERR_DTYPE / CP_ERR_ARG).  launch = -1: delta;
+ * launch = 0: the dK/dV kernel over every ring step -- each KV tile stays
+ * put while the query chunks that see it stream past in the order the
+ * ring's steps bring them to its holder, its dK / dV held in TMEM and
+ * written once; launch = 1: the dQ kernel over every step -- each query
+ * tile walks the KV chunks its rank holds at steps 0 .. P-1, as the
+ * forward's one-launch ring does.  Same gradients as the per-step schedule
+ * up to rounding (the same terms summed in another grouping).
  */
 int cp_ring_backward_step(const void* q, const void* k, const void* v, const void* out,
                           const void* dout, const float* lse, cp_dtype in_dt, int64_t S, int H,
                           int Hkv, int D, int P, cp_layout layout, int launch, void* dq,
                           void* dk, void* dv, cp_dtype grad_dt, void* workspace,
                           cp_stream_t stream);
+int cp_ring_backward_fused_step(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse, cp_dtype in_dt, int64_t S,
+                                int H, int Hkv, int D, int P, cp_layout layout, int launch,
+                                void* dq, void* dk, void* dv, cp_dtype grad_dt, void* workspace,
+                                cp_stream_t stream);
 int cp_ring_backward(const void* q, const void* k, const void* v, const void* out,
                      const void* dout, const float* lse, cp_dtype in_dt, int64_t S, int H,
                      int Hkv, int D, int P, cp_layout layout, void* dq, void* dk, void* dv,

@@ -262,21 +262,49 @@ def test_ring_backward_matches_block_sum(cp):
         assert diff <= 1e-4 * want.abs().max().item(), f"{name}: ring vs block sum {diff:.3e}"
 
 
-def test_ring_backward_steps_equal_whole(cp):
-    """cp_ring_backward_step over launches -1 .. 2P-1 is cp_ring_backward,
-    bit for bit (the same kernels in the same order)."""
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+def test_ring_backward_steps_equal_whole(cp, layout):
+    """cp_ring_backward (bf16: two launches over every step) is
+    cp_ring_backward_fused_step over launches -1, 0, 1, bit for bit; the
+    per-step schedule (cp_ring_backward_step over -1 .. 2P-1) gives the same
+    gradients within the derived tolerance and against the oracle."""
     S, H, P = 2048, 2, 4
     q, k, v, do, ob, l32 = forward_inputs(S, H, 1, seed=41)
     args = dev(q, k, v, ob, do, l32)
-    a = cp.cp_ring_backward(*args, P, "zigzag", grad_dtype=torch.bfloat16)
+    a = cp.cp_ring_backward(*args, P, layout, grad_dtype=torch.bfloat16)
     ws = torch.empty(cp.cp_ring_backward_workspace_size(S, H, 1, 128, torch.bfloat16),
                      dtype=torch.uint8, device="cuda")
     b = [torch.empty_like(t) for t in a]
+    for launch in (-1, 0, 1):
+        cp.cp_ring_backward_fused_step(*args, P, layout, launch, *b, ws)
+    c = [torch.empty_like(t) for t in a]
     for launch in range(-1, 2 * P):
-        cp.cp_ring_backward_step(*args, P, "zigzag", launch, *b, ws)
+        cp.cp_ring_backward_step(*args, P, layout, launch, *c, ws)
     cp.cp_check_device_error()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+    for got, want, name in zip(c, oracle_grads(q, k, v, do, ob, l32), ("dq", "dk", "dv")):
+        grads_close(got, want, name + " (per step)")
+
+
+@pytest.mark.parametrize("layout,S,P,Hkv", [("zigzag", 4096, 8, 2), ("zigzag", 4096, 16, 4),
+                                            ("contiguous", 4096, 8, 4), ("zigzag", 1000, 3, 2),
+                                            ("contiguous", 1500, 4, 1), ("zigzag", 300, 8, 4),
+                                            ("zigzag", 2048, 1, 4)])
+def test_ring_backward_fused_against_oracle(cp, layout, S, P, Hkv):
+    """The two-launch ring backward (every step inside one dK/dV and one dQ
+    launch) against the oracle's monolithic gradients: degrees 1..16, GQA
+    4:1 .. 4:4, chunks that are not multiples of the 128-row tile, a short
+    last chunk; guard bands around the gradients."""
+    q, k, v, do, ob, l32 = forward_inputs(S, 4, Hkv, seed=S + P + Hkv)
+    (dq, dq_ok), (dk, dk_ok), (dv, dv_ok) = (guarded(t.shape, torch.float32) for t in (q, k, v))
+    cp.cp_ring_backward(*dev(q, k, v, ob, do, l32), P, layout, dq=dq, dk=dk, dv=dv)
+    cp.cp_check_device_error()
+    rq, rk, rv = oracle_grads(q, k, v, do, ob, l32)
+    grads_close(dq, rq, "dq")
+    grads_close(dk, rk, "dk")
+    grads_close(dv, rv, "dv")
+    assert dq_ok() and dk_ok() and dv_ok(), "write outside dq / dk / dv"
 
 
 # ------------------------------------------------- full size, sampled rows
