@@ -138,13 +138,18 @@ int launch_items(Launch& L, cp_dtype in_dt, const void* q, int64_t q_rows, const
   if (static_cast<int>(L.items.size()) > kMaxItems)
     return fail(CP_ERR_ARG, "too many work items (%d)", int(L.items.size()));
   p.nitems = static_cast<int>(L.items.size());
-  int64_t total = 0;
+  int64_t total = 0, tiles = 0;
   for (int i = 0; i < p.nitems; ++i) {
     p.items[i] = L.items[i];
     if (p.items[i].o_stride == 0) p.items[i].o_stride = 1;  // plain rows by default
     p.cta_start[i] = static_cast<int>(total);
+    p.tile_start[i] = static_cast<int>(tiles);
     total += in_dt == CP_BF16 ? attn_tc_ctas(L.items[i], p.H) : attn_simt_ctas(L.items[i], p.H);
+    tiles += attn_tc_ctas(L.items[i], 1) / L.items[i].batch;
   }
+  p.tile_start[p.nitems] = static_cast<int>(tiles);
+  if (p.head_major && (in_dt != CP_BF16 || total != tiles * p.H))
+    return fail(CP_ERR_ARG, "head-major launch needs bf16 items of batch 1");
   if (total > 0x7fffffff) return fail(CP_ERR_SHAPE, "grid too large");
   p.cta_start[p.nitems] = static_cast<int>(total);
   for (int i = p.nitems + 1; i <= kMaxItems; ++i) p.cta_start[i] = static_cast<int>(total);
@@ -412,6 +417,17 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
               out_dt == CP_F32 ? static_cast<float*>(out) : nullptr, lse, S);
   L.p.ring_C = C;
   L.p.ring_S = S;
+  // Every query tile walks its head's whole visible K/V.  When all heads' K/V
+  // is more than half of L2, run the grid head by head so that the CTAs
+  // resident at one time share one head's K/V (at 32K this cut DRAM reads
+  // from 4.8 GB to 0.83 GB per launch); otherwise keep the items'
+  // longest-first order across all heads, which ends with a shorter tail
+  // (4K: 954 against 767 TFLOP/s head by head).
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+    l2 = 0;
+  L.p.head_major = S * Hkv * static_cast<int64_t>(D) * 2 * 2 > static_cast<int64_t>(l2) / 2;
   std::vector<int64_t> work;  // visible keys x rows, for the longest-first order
   for (int r = 0; r < P; ++r) {
     int qcs[2];

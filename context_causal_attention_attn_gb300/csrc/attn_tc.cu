@@ -123,15 +123,28 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
   if (threadIdx.x == 0) grid_launch_dependents();
 
   // ---------------------------------------------------------- task decode
-  int ii = 0;
-  while (ii + 1 < p.nitems && static_cast<int>(blockIdx.x) >= p.cta_start[ii + 1]) ++ii;
-  const WorkItem& it = p.items[ii];
-  int local = static_cast<int>(blockIdx.x) - p.cta_start[ii];
-  const int npairs = (it.sq + NT * tc::BM - 1) / (NT * tc::BM);
-  // query-tile groups vary fastest: the CTAs resident at one time share a
-  // head (and its K/V), which then stays in L2
-  const int pair = npairs - 1 - local % npairs;  // later query rows (more keys) first
-  local /= npairs;
+  int ii = 0, pair, local;
+  const WorkItem* itp;
+  if (p.head_major) {
+    // head by head; within a head the items in order, later query tiles first
+    const int tiles = p.tile_start[p.nitems];
+    const int r = static_cast<int>(blockIdx.x) % tiles;
+    local = static_cast<int>(blockIdx.x) / tiles;
+    while (ii + 1 < p.nitems && r >= p.tile_start[ii + 1]) ++ii;
+    itp = &p.items[ii];
+    const int npairs = (itp->sq + NT * tc::BM - 1) / (NT * tc::BM);
+    pair = npairs - 1 - (r - p.tile_start[ii]);
+  } else {
+    while (ii + 1 < p.nitems && static_cast<int>(blockIdx.x) >= p.cta_start[ii + 1]) ++ii;
+    itp = &p.items[ii];
+    local = static_cast<int>(blockIdx.x) - p.cta_start[ii];
+    const int npairs = (itp->sq + NT * tc::BM - 1) / (NT * tc::BM);
+    // query-tile groups vary fastest: the CTAs resident at one time share a
+    // head (and its K/V), which then stays in L2
+    pair = npairs - 1 - local % npairs;  // later query rows (more keys) first
+    local /= npairs;
+  }
+  const WorkItem& it = *itp;
   const int head = local % p.H;
   const int b = local / p.H;
   const int row0 = pair * NT * tc::BM;

@@ -107,6 +107,12 @@ struct AttnParams {
   const void* v;
   int64_t q_rows, k_rows;      // rows of the q / k tensors (bounds)
   int64_t ring_C, ring_S;      // chunk rows and sequence length of chunk-list items
+  // head_major: the grid runs head by head (all items' query tiles of head 0,
+  // then head 1, ...), so the CTAs resident at one time read one head's K/V;
+  // tile_start is the prefix sum of query tiles per item.  Otherwise item by
+  // item (cta_start), query tiles fastest within a head.
+  int head_major;
+  int tile_start[kMaxItems + 1];
 };
 
 // Status word written by kernels whose bounded wait expired.
