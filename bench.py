@@ -425,9 +425,16 @@ def run_gpu(args, wl, rank, world, local):
     elif wl["kind"] == "usp":
         ws = torch.empty(cp.cp_usp_workspace_size(S, H, Hkv, D, torch.bfloat16, torch.bfloat16),
                          dtype=torch.uint8, device=dev)
-        launches_per_step = 4 + wl["Pr"]  # 3 permutes, Pr ring steps, inverse permute
-        stages = list(range(wl["Pr"] + 2))  # permutes, ring steps 1..Pr, inverse permute
-        attn_stages = set(range(1, wl["Pr"] + 1))
+        if cp.ring_runs_fused(q, layout):
+            # the whole ring is stage 1 (one launch); stages 2..Pr launch nothing
+            launches_per_step = 5  # 3 permutes, the ring, inverse permute
+            stages, attn_stages = [0, 1, wl["Pr"] + 1], {1}
+            ring_impl = (f"cp_usp_forward: the rings of all {wl['Pu']} head groups, all "
+                         f"{wl['Pr']} steps, in one launch")
+        else:
+            launches_per_step = 4 + wl["Pr"]  # 3 permutes, Pr ring steps, inverse permute
+            stages = list(range(wl["Pr"] + 2))  # permutes, ring steps 1..Pr, inverse permute
+            attn_stages = set(range(1, wl["Pr"] + 1))
 
         def launch(st):
             cp.cp_usp_stage(q, k, v, wl["Pu"], wl["Pr"], layout, st, out, lse, ws, stream=stream)

@@ -148,8 +148,13 @@ int launch_items(Launch& L, cp_dtype in_dt, const void* q, int64_t q_rows, const
     tiles += attn_tc_ctas(L.items[i], 1) / L.items[i].batch;
   }
   p.tile_start[p.nitems] = static_cast<int>(tiles);
-  if (p.head_major && (in_dt != CP_BF16 || total != tiles * p.H))
-    return fail(CP_ERR_ARG, "head-major launch needs bf16 items of batch 1");
+  if (p.head_major) {
+    // the grid is tiles x (heads x batch): every item has the same batch
+    bool uniform = in_dt == CP_BF16;
+    for (int i = 1; i < p.nitems; ++i) uniform = uniform && p.items[i].batch == p.items[0].batch;
+    if (!uniform || total != tiles * p.H * p.items[0].batch)
+      return fail(CP_ERR_ARG, "head-major launch needs bf16 items of one batch size");
+  }
   if (total > 0x7fffffff) return fail(CP_ERR_SHAPE, "grid too large");
   p.cta_start[p.nitems] = static_cast<int>(total);
   for (int i = p.nitems + 1; i <= kMaxItems; ++i) p.cta_start[i] = static_cast<int>(total);
@@ -403,10 +408,12 @@ int ring_step_impl(const void* q, const void* k, const void* v, cp_dtype in_dt, 
 // tile carries its running max, sum and output in TMEM from one step to the
 // next (the online-softmax form of the LSE merge) and writes the final
 // result once, so no accumulator round trip, per-step epilogue or launch
-// separates the steps.
+// separates the steps.  With `rb` the launch covers a batch of independent
+// sequences (the head groups of USP), each its own ring.
 int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int H, int Hkv,
                     int D, int P, cp_layout layout, void* out, cp_dtype out_dt, float* lse,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, const RingBatch* rb = nullptr) {
+  const int64_t q_rows = rb ? rb->q_rows : S, k_rows = rb ? rb->k_rows : S;
   const int64_t nchunks = layout == CP_ZIGZAG ? 2 * P : P;
   const int64_t C = (S + nchunks - 1) / nchunks;
   auto chunk_rows = [&](int64_t c) -> int64_t {
@@ -417,6 +424,10 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
               out_dt == CP_F32 ? static_cast<float*>(out) : nullptr, lse, S);
   L.p.ring_C = C;
   L.p.ring_S = S;
+  if (rb) {
+    L.p.b_q_heads = rb->b_q_heads;
+    L.p.kv_group = rb->kv_group;
+  }
   // Every query tile walks its head's whole visible K/V.  When all heads' K/V
   // is more than half of L2, run the grid head by head so that the CTAs
   // resident at one time share one head's K/V (at 32K this cut DRAM reads
@@ -427,7 +438,7 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
     l2 = 0;
-  L.p.head_major = S * Hkv * static_cast<int64_t>(D) * 2 * 2 > static_cast<int64_t>(l2) / 2;
+  L.p.head_major = k_rows * Hkv * static_cast<int64_t>(D) * 2 * 2 > static_cast<int64_t>(l2) / 2;
   std::vector<int64_t> work;  // visible keys x rows, for the longest-first order
   for (int r = 0; r < P; ++r) {
     int qcs[2];
@@ -442,6 +453,13 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
       w.lse_col = qc * C;
       w.sq = static_cast<int32_t>(chunk_rows(qc));
       w.batch = 1;
+      if (rb) {
+        w.batch = rb->batch;
+        w.b_q_rows = rb->b_q_rows;
+        w.b_k_rows = rb->b_k_rows;
+        w.b_o_rows = rb->b_o_rows;
+        w.b_lse_heads = rb->b_lse_heads;
+      }
       w.flags = kFlagCausal | kFlagFinal;
       int64_t keys = 0;
       for (int t = 0; t < P; ++t) {
@@ -467,7 +485,7 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
   std::vector<WorkItem> sorted;
   for (size_t i : order) sorted.push_back(L.items[i]);
   L.items.swap(sorted);
-  return launch_items(L, CP_BF16, q, S, k, v, S, stream);
+  return launch_items(L, CP_BF16, q, q_rows, k, v, k_rows, stream);
 }
 
 // Copy-mode ring: one D2D copy per rank and tensor moves every rank's held
@@ -1483,7 +1501,10 @@ static int ulysses_host_impl(const void* hq, const void* hk, const void* hv, cp_
     char* q_p = ws + st.q + p * rows * qw;
     char* k_p = ws + st.k + p * rows * kw;
     char* v_p = ws + st.v + p * rows * kw;
-    if (Pr > 0) {
+    if (Pr > 0 && ring_runs_fused(in_dt, layout)) {
+      rc = ring_fused_impl(q_p, k_p, v_p, S, G, Gkv, D, Pr, layout, out_p, out_dt, lse_p, cs);
+      if (rc != CP_OK) return rc;
+    } else if (Pr > 0) {
       for (int t = 0; t < Pr; ++t) {
         rc = ring_step_impl(q_p, k_p, v_p, in_dt, S, G, Gkv, D, Pr, layout, t, out_p, out_dt,
                             lse_p, ws + st.acc, cs, nullptr, nullptr, t > 0);
@@ -1596,12 +1617,21 @@ static int usp_impl(const void* q, const void* k, const void* v, cp_dtype in_dt,
   rb.kv_group = replicate ? H / Hkv : G / Gkv;
   rb.q_rows = Pu * S;
   rb.k_rows = replicate ? S : Pu * S;
-  for (int t = 0; t < Pr; ++t) {
-    if (stage > 0 && stage != t + 1) continue;
-    // a step overlaps the previous one only when both run in this call
-    rc = ring_step_impl(qh, replicate ? k : kh, replicate ? v : vh, in_dt, S, G, Gkv, D, Pr, layout,
-                        t, oh, out_dt, lse, acc, s, nullptr, &rb, stage < 0 && t > 0);
-    if (rc != CP_OK) return rc;
+  if (ring_runs_fused(in_dt, layout)) {
+    // the whole ring in one launch (stage 1; stages 2 .. Pr have nothing left)
+    if (stage < 0 || stage == 1) {
+      rc = ring_fused_impl(qh, replicate ? k : kh, replicate ? v : vh, S, G, Gkv, D, Pr, layout,
+                           oh, out_dt, lse, s, &rb);
+      if (rc != CP_OK) return rc;
+    }
+  } else {
+    for (int t = 0; t < Pr; ++t) {
+      if (stage > 0 && stage != t + 1) continue;
+      // a step overlaps the previous one only when both run in this call
+      rc = ring_step_impl(qh, replicate ? k : kh, replicate ? v : vh, in_dt, S, G, Gkv, D, Pr,
+                          layout, t, oh, out_dt, lse, acc, s, nullptr, &rb, stage < 0 && t > 0);
+      if (rc != CP_OK) return rc;
+    }
   }
   if (stage > 0) return ok();
   if ((rc = cp_head_to_seq(oh, out, out_dt, S, H, D, Pu, stream)) != CP_OK) return rc;

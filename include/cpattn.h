@@ -399,8 +399,10 @@ int cp_ulysses_stage(const void* q, const void* k, const void* v, cp_dtype in_dt
  *   [CP-handbook] section "怎么选" (Ulysses inside a node and Ring across
  *   nodes, the USP scheme).  seq_to_head with degree Pu (KV heads replicated
  *   in place when Pu is a multiple of Hkv), then the ring of cp_ring_forward
- *   with Pr ranks and `layout` over each group's whole sequence (one launch
- *   per ring step covers all Pu groups), then head_to_seq.
+ *   with Pr ranks and `layout` over each group's whole sequence, then
+ *   head_to_seq.  The rings of all Pu groups share each launch: one launch
+ *   for the whole ring where cp_ring_forward runs in one (bf16 inputs,
+ *   contiguous or zigzag), else one per ring step.
  *   The same arguments as cp_ulysses_forward plus Pr and layout; S % Pu = 0
  *   and the ring's own conditions on (S, Pr, layout).
  *   workspace: cp_usp_workspace_size() bytes.
@@ -414,9 +416,10 @@ int cp_usp_forward(const void* q, const void* k, const void* v, cp_dtype in_dt, 
 /*
  * cp_usp_stage - one stage of cp_usp_forward (same arguments plus `stage`):
  * 0 = seq_to_head of q, k, v, 1 .. Pr = ring step stage-1 (one launch over
- * all Pu groups), Pr + 1 = head_to_seq of the output.  Stages 0 .. Pr + 1 in
- * order on one stream are cp_usp_forward, bit for bit.  Other stages:
- * CP_ERR_ARG.
+ * all Pu groups), Pr + 1 = head_to_seq of the output.  Where the ring runs
+ * in one launch (bf16 inputs, contiguous or zigzag), stage 1 is the whole
+ * ring and stages 2 .. Pr launch nothing.  Stages 0 .. Pr + 1 in order on
+ * one stream are cp_usp_forward, bit for bit.  Other stages: CP_ERR_ARG.
  */
 int cp_usp_stage(const void* q, const void* k, const void* v, cp_dtype in_dt, int64_t S,
                  int H, int Hkv, int D, int Pu, int Pr, cp_layout layout, void* out,

@@ -206,10 +206,12 @@ def test_ring_deterministic(cp, qkv4k):
 
 
 # -------------------------------------------------------- long, sampled rows
-def _sampled_check(cp, S, H, Hkv, P, layout, n_rows=512, ulysses=False):
+def _sampled_check(cp, S, H, Hkv, P, layout, n_rows=512, ulysses=False, usp_Pu=0):
     q, k, v = make_qkv(S, H, 128, Hkv=Hkv, dtype=torch.bfloat16, device="cuda")
     if ulysses:
         out, lse = cp.cp_ulysses_forward(q, k, v, P)
+    elif usp_Pu:
+        out, lse = cp.cp_usp_forward(q, k, v, usp_Pu, P, layout)
     else:
         out, lse = cp.cp_ring_forward(q, k, v, P, layout)
     cp.cp_check_device_error()
@@ -239,6 +241,13 @@ def test_ring_128k_sampled(cp, layout):
 def test_ulysses_64k_gqa_sampled(cp):
     """S=65536, 32 query / 8 KV heads, P=8 (one KV head per virtual rank)."""
     _sampled_check(cp, 65536, 32, 8, 8, "contiguous", ulysses=True)
+
+
+def test_usp_64k_gqa_sampled(cp):
+    """S=65536, 32 query / 8 KV heads, Ulysses over 4 head groups x a zigzag
+    ring of 2 in each: the four groups' rings share one launch, run head by
+    head (the groups' K/V is more than half of L2)."""
+    _sampled_check(cp, 65536, 32, 8, 2, "zigzag", usp_Pu=4)
 
 
 # ------------------------------------------------------------ Ulysses small
@@ -395,6 +404,7 @@ def test_ring_copy_mode_fp32_toy(cp):
 # ------------------------------------------------------------- USP hybrid
 @pytest.mark.parametrize("S,H,Hkv,Pu,Pr,layout", [(1024, 32, 8, 4, 2, "zigzag"),
                                                   (1024, 16, 2, 4, 2, "striped"),
+                                                  (1024, 16, 2, 4, 2, "zigzag"),
                                                   (1000, 8, 4, 2, 3, "contiguous"),
                                                   (2048, 32, 8, 8, 4, "zigzag")])
 def test_usp_bf16(cp, S, H, Hkv, Pu, Pr, layout):
