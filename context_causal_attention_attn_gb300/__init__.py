@@ -8,10 +8,10 @@ marshal torch tensors into the C ABI declared in include/cpattn.h; all
 computation happens in the library's CUDA kernels.
 """
 
-from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_ERR_TIMEOUT, CP_F32, CP_MAX_RANKS, CP_STRIPED,
+from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_ERR_BOUNDS, CP_ERR_TIMEOUT, CP_F32, CP_MAX_RANKS, CP_STRIPED,
                    CP_ZIGZAG, CpError, cp_attn_block, cp_attn_block_backward,
-                   cp_attn_block_backward_workspace_size, cp_check_device_error, cp_head_to_seq,
-                   cp_last_error, cp_lse_merge, cp_ring_backward, cp_ring_backward_host,
+                   cp_attn_block_backward_workspace_size, cp_check_device_error, cp_debug_bounds,
+                   cp_head_to_seq, cp_last_error, cp_lse_merge, cp_ring_backward, cp_ring_backward_host,
                    cp_ring_backward_host_workspace_size, cp_ring_backward_step,
                    cp_ring_backward_workspace_size, cp_ring_copy_workspace_size, cp_ring_forward,
                    cp_ring_forward_copy, cp_ring_forward_fused, cp_ring_forward_host,
@@ -24,10 +24,11 @@ from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_ERR_TIMEOUT, CP_F32, CP_MAX_RANKS,
                    cp_usp_workspace_size, cp_version, lib, library_path)
 
 __all__ = [
-    "CP_BF16", "CP_CONTIGUOUS", "CP_ERR_TIMEOUT", "CP_F32", "CP_MAX_RANKS",
+    "CP_BF16", "CP_CONTIGUOUS", "CP_ERR_BOUNDS", "CP_ERR_TIMEOUT", "CP_F32", "CP_MAX_RANKS",
     "CP_STRIPED",
     "CP_ZIGZAG", "CpError", "cp_attn_block", "cp_attn_block_backward",
-    "cp_attn_block_backward_workspace_size", "cp_check_device_error", "cp_head_to_seq",
+    "cp_attn_block_backward_workspace_size", "cp_check_device_error", "cp_debug_bounds",
+    "cp_head_to_seq",
     "cp_last_error", "cp_lse_merge", "cp_ring_backward", "cp_ring_backward_host",
     "cp_ring_backward_host_workspace_size", "cp_ring_backward_step",
     "cp_ring_backward_workspace_size", "cp_ring_copy_workspace_size", "cp_ring_forward",

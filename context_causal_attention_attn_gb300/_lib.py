@@ -18,8 +18,9 @@ CP_F32, CP_BF16 = 0, 1
 CP_CONTIGUOUS, CP_ZIGZAG, CP_STRIPED = 0, 1, 2
 CP_MAX_RANKS = 16
 STATUS = {0: "CP_OK", -1: "CP_ERR_ARG", -2: "CP_ERR_SHAPE", -3: "CP_ERR_DTYPE",
-          -4: "CP_ERR_ALIGN", -5: "CP_ERR_CUDA", -6: "CP_ERR_TIMEOUT"}
+          -4: "CP_ERR_ALIGN", -5: "CP_ERR_CUDA", -6: "CP_ERR_TIMEOUT", -7: "CP_ERR_BOUNDS"}
 CP_ERR_TIMEOUT = -6
+CP_ERR_BOUNDS = -7
 
 _LIB = None
 
@@ -30,19 +31,27 @@ class CpError(RuntimeError):
         self.code = code
 
 
+def debug_requested():
+    """CPATTN_DEBUG=1 selects the bounds-checked library."""
+    return os.environ.get("CPATTN_DEBUG", "0") not in ("", "0")
+
+
 def library_path():
-    return _build.LIB
+    return _build.lib_path(debug_requested())
 
 
 def lib():
-    """Load libcpattn.so (built in-tree by ``build.build()``)."""
+    """Load libcpattn.so (built in-tree by ``build.build()``), or with
+    CPATTN_DEBUG=1 the bounds-checked libcpattn_debug.so
+    (``build.build(debug=True)``)."""
     global _LIB
     if _LIB is not None:
         return _LIB
     path = library_path()
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with "
-                           "context_causal_attention_attn_gb300.build.build()")
+                           "context_causal_attention_attn_gb300.build.build(" +
+                           ("debug=True)" if debug_requested() else ")"))
     L = ctypes.CDLL(path)
     vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
     sig = {
@@ -100,6 +109,7 @@ def lib():
                                               i32, i32, i32, vp, vp, vp, i32, vp, vp]),
         "cp_check_device_error": (i32, [vp]),
         "cp_selftest_wait_timeout": (i32, [i32, vp]),
+        "cp_debug_bounds": (i32, []),
         "cp_last_error": (ctypes.c_char_p, []),
         "cp_version": (ctypes.c_char_p, []),
     }
@@ -709,8 +719,14 @@ def cp_ring_backward_fused_step(q, k, v, out, dout, lse, P, layout, launch, dq, 
 
 def cp_check_device_error(stream=None):
     """Synchronise the stream; raise CpError(CP_ERR_TIMEOUT) if a kernel's
-    bounded wait expired since the last check."""
+    bounded wait expired since the last check (CP_ERR_BOUNDS: a bounds check
+    of the bounds-checked library failed)."""
     return _check(lib().cp_check_device_error(_stream(stream)))
+
+
+def cp_debug_bounds():
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().cp_debug_bounds())
 
 
 def cp_selftest_wait_timeout(timeout_us=2000, stream=None):

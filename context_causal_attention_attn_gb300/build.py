@@ -7,7 +7,13 @@ are serialised across processes by an exclusive lock on ``_build/.lock``, so
 several processes (ranks of one job, test workers) may call build() at once:
 the first compiles, the others wait and find the library up to date.
 
-    python -m context_causal_attention_attn_gb300.build [--force]
+``build(debug=True)`` makes the bounds-checked library ``libcpattn_debug.so``
+instead (sources compiled with ``-DCP_DEBUG_BOUNDS`` into ``_build/debug/``):
+its kernels check every tile and row they touch against the tensors' extents
+and report a failure through ``cp_check_device_error``.  The binding loads it
+in place of the release library when the environment has ``CPATTN_DEBUG=1``.
+
+    python -m context_causal_attention_attn_gb300.build [--force] [--debug]
 """
 
 import concurrent.futures as cf
@@ -25,6 +31,13 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcpattn.so")
+LIB_DEBUG = os.path.join(PKG, "libcpattn_debug.so")
+DEBUG_FLAGS = ["-DCP_DEBUG_BOUNDS"]
+
+
+def lib_path(debug=False):
+    return LIB_DEBUG if debug else LIB
+
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -47,16 +60,20 @@ def _deps():
         os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(debug=False):
+    lib = lib_path(debug)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    cmd = [nvcc()] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
+def _compile(src, extra, debug=False):
+    obj_dir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(obj_dir, exist_ok=True)
+    obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + (DEBUG_FLAGS if debug else []) + extra + [
+        "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
@@ -74,36 +91,39 @@ def _locked():
             fcntl.flock(f, fcntl.LOCK_UN)
 
 
-def build(force=False, verbose=False, extra=()):
-    """Compile and link; returns the path of the library."""
-    if not force and up_to_date():
-        return LIB
+def build(force=False, verbose=False, extra=(), debug=False):
+    """Compile and link; returns the path of the library (the bounds-checked
+    one with debug=True)."""
+    if not force and up_to_date(debug):
+        return lib_path(debug)
     with _locked():
-        if not force and up_to_date():
-            return LIB
-        return _build(verbose, extra)
+        if not force and up_to_date(debug):
+            return lib_path(debug)
+        return _build(verbose, extra, debug)
 
 
-def _build(verbose, extra):
+def _build(verbose, extra, debug=False):
     extra = list(extra)
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), sources()))
+        results = list(ex.map(lambda s: _compile(s, extra, debug), sources()))
     objs = [o for o, _ in results]
     if verbose:
         for _, err in results:
             if err:
                 sys.stderr.write(err)
-    tmp = LIB + ".tmp"
+    lib = lib_path(debug)
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     force = "--force" in sys.argv
     verbose = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []
-    print(build(force=force or bool(extra), verbose=verbose or bool(extra), extra=extra))
+    print(build(force=force or bool(extra), verbose=verbose or bool(extra), extra=extra,
+                debug="--debug" in sys.argv))

@@ -20,7 +20,7 @@ cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const AttnParams& p, int ctas, int* dev_err, cudaStream_t stream,
                            bool dependent);
 int attn_tc_ctas(const WorkItem& it, int H);
-cudaError_t launch_attn_simt(const AttnParams& p, int ctas, cudaStream_t stream);
+cudaError_t launch_attn_simt(const AttnParams& p, int ctas, int* dev_err, cudaStream_t stream);
 int attn_simt_ctas(const WorkItem& it, int H);
 cudaError_t launch_lse_merge(float* out_acc, float* lse_acc, const float* out_blk,
                              const float* lse_blk, int64_t Sq, int H, int D, cudaStream_t s);
@@ -37,7 +37,7 @@ int attn_bwd_ctas(const BwdItem& it, int heads);
 int attn_bwd_simt_warps(const BwdItem& it, int heads);
 cudaError_t launch_attn_bwd_simt(bool dkdv, const void* q, const void* k, const void* v,
                                  const void* dout, const BwdParams& p, int D, int warps,
-                                 cudaStream_t s);
+                                 int* dev_err, cudaStream_t s);
 cudaError_t launch_bwd_delta_f32(const void* out, const void* dout, float* delta, int64_t rows,
                                  int H, int D, int64_t ld, cudaStream_t s);
 cudaError_t launch_bwd_delta(const void* out, const void* dout, float* delta, int64_t rows, int H,
@@ -180,7 +180,9 @@ int launch_items(Launch& L, cp_dtype in_dt, const void* q, int64_t q_rows, const
     if (st == nullptr) return fail(CP_ERR_CUDA, "device status word unavailable");
     e = launch_attn_tc(tq, tk, tv, p, static_cast<int>(total), st, stream, dependent);
   } else {
-    e = launch_attn_simt(p, static_cast<int>(total), stream);
+    int* st = device_status_ptr();
+    if (st == nullptr) return fail(CP_ERR_CUDA, "device status word unavailable");
+    e = launch_attn_simt(p, static_cast<int>(total), st, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   return CP_OK;
@@ -629,6 +631,8 @@ int run_bwd_task(const BwdArgs& a, const BwdTask& t, const CUtensorMap maps[4], 
   p.ld = a.ld;
   p.ring_C = t.ring_C;
   p.ring_S = t.ring_S;
+  p.q_rows = a.q_rows;
+  p.k_rows = a.k_rows;
   if (t.dkdv) {
     p.acc0 = a.acc_v;
     p.acc1 = a.acc_k;
@@ -652,13 +656,13 @@ int run_bwd_task(const BwdArgs& a, const BwdTask& t, const CUtensorMap maps[4], 
   if (total > 0x7fffffff) return fail(CP_ERR_SHAPE, "grid too large");
   for (int i = p.nitems; i <= kMaxItems; ++i) p.cta_start[i] = static_cast<int>(total);
   if (total == 0) return CP_OK;
-  if (f32) {
-    cudaError_t e = launch_attn_bwd_simt(t.dkdv, a.q, a.k, a.v, a.dout, p, a.D,
-                                         static_cast<int>(total), s);
-    return e == cudaSuccess ? CP_OK : cuda_fail(e, "backward kernel launch");
-  }
   int* st = device_status_ptr();
   if (st == nullptr) return fail(CP_ERR_CUDA, "device status word unavailable");
+  if (f32) {
+    cudaError_t e = launch_attn_bwd_simt(t.dkdv, a.q, a.k, a.v, a.dout, p, a.D,
+                                         static_cast<int>(total), st, s);
+    return e == cudaSuccess ? CP_OK : cuda_fail(e, "backward kernel launch");
+  }
   cudaError_t e = launch_attn_bwd(t.dkdv, maps[0], maps[1], maps[2], maps[3], p,
                                   static_cast<int>(total), st, s);
   return e == cudaSuccess ? CP_OK : cuda_fail(e, "backward kernel launch");
@@ -1924,10 +1928,20 @@ int cp_check_device_error(cp_stream_t stream) {
     const int zero = 0;
     e = cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    if ((v & 0xff) == kDevErrBounds) {
+      static const char* const sites[] = {
+          "?", "forward query tile", "forward K/V tile", "fp32 forward row",
+          "backward stationary tile", "backward streamed tile", "fp32 backward row"};
+      const int site = v >> 8;
+      return fail(CP_ERR_BOUNDS, "a device-side bounds check failed: %s (site %d)",
+                  sites[site >= 1 && site <= 6 ? site : 0], site);
+    }
     return fail(CP_ERR_TIMEOUT, "a device-side wait expired (status %d)", v);
   }
   return ok();
 }
+
+int cp_debug_bounds(void) { return kDebugBounds ? 1 : 0; }
 
 int cp_selftest_wait_timeout(int timeout_us, cp_stream_t stream) {
   if (timeout_us < 1 || timeout_us > 2000000) return fail(CP_ERR_ARG, "timeout_us out of range");

@@ -77,7 +77,7 @@ template <int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     bwd_dq_simt_kernel(const float* __restrict__ q, const float* __restrict__ k,
                        const float* __restrict__ v, const float* __restrict__ dout,
-                       BwdParams p) {
+                       BwdParams p, int* dev_err) {
   constexpr int E = (D + 31) / 32;
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -91,6 +91,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int kvh = h / (p.H / p.Hkv);
   const int64_t tok = seg_token(it.stat, r, p.stride);
   const int64_t qpos = it.stat.pos + r;
+  // bounds-checked build: the query row (also its lse / delta column and
+  // dq row) lies inside its tensors
+  if (kDebugBounds && !bounds_ok(tok >= 0 && tok < p.q_rows && tok < p.ld && h < p.H,
+                                 dev_err, kSiteBwdSimt))
+    return;
   float qi[E], doi[E], dq[E];
   load_vec<D>(q + (tok * p.H + h) * D, qi, lane);
   load_vec<D>(dout + (tok * p.H + h) * D, doi, lane);
@@ -104,6 +109,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       for (int j = 0; j < g.len; ++j) {
         if (p.causal && g.pos + j > qpos) break;
         const int64_t kt = seg_token(g, j, p.stride);
+        if (kDebugBounds && !bounds_ok(kt >= 0 && kt < p.k_rows, dev_err, kSiteBwdSimt)) break;
         float kj[E], vj[E];
         load_vec<D>(k + (kt * p.Hkv + kvh) * D, kj, lane);
         load_vec<D>(v + (kt * p.Hkv + kvh) * D, vj, lane);
@@ -121,7 +127,7 @@ template <int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     bwd_dkdv_simt_kernel(const float* __restrict__ q, const float* __restrict__ k,
                          const float* __restrict__ v, const float* __restrict__ dout,
-                         BwdParams p) {
+                         BwdParams p, int* dev_err) {
   constexpr int E = (D + 31) / 32;
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -135,6 +141,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int grp = p.H / p.Hkv;
   const int64_t tok = seg_token(it.stat, r, p.stride);
   const int64_t kpos = it.stat.pos + r;
+  // bounds-checked build: the key row (also its dk / dv row) lies inside
+  // its tensors
+  if (kDebugBounds &&
+      !bounds_ok(tok >= 0 && tok < p.k_rows && kvh < p.Hkv, dev_err, kSiteBwdSimt))
+    return;
   float kj[E], vj[E], dk[E], dv[E];
   load_vec<D>(k + (tok * p.Hkv + kvh) * D, kj, lane);
   load_vec<D>(v + (tok * p.Hkv + kvh) * D, vj, lane);
@@ -147,6 +158,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       for (int i = 0; i < seg.len; ++i) {
         if (p.causal && seg.pos + i < kpos) continue;
         const int64_t qt = seg_token(seg, i, p.stride);
+        if (kDebugBounds &&
+            !bounds_ok(qt >= 0 && qt < p.q_rows && qt < p.ld, dev_err, kSiteBwdSimt))
+          break;
         const float lse = p.lse[static_cast<int64_t>(h) * p.ld + qt];
         if (lse == -CUDART_INF_F) continue;
         const float dl = p.delta[static_cast<int64_t>(h) * p.ld + qt];
@@ -198,11 +212,11 @@ cudaError_t dispatch_d(int D, A... a) {
 template <int D>
 struct RunDq {
   static cudaError_t run(const void* q, const void* k, const void* v, const void* dout,
-                         const BwdParams* p, int warps, cudaStream_t s) {
+                         const BwdParams* p, int warps, int* dev_err, cudaStream_t s) {
     const int blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     bwd_dq_simt_kernel<D><<<blocks, kWarpsPerBlock * 32, 0, s>>>(
         static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
-        static_cast<const float*>(dout), *p);
+        static_cast<const float*>(dout), *p, dev_err);
     return cudaGetLastError();
   }
 };
@@ -210,11 +224,11 @@ struct RunDq {
 template <int D>
 struct RunDkdv {
   static cudaError_t run(const void* q, const void* k, const void* v, const void* dout,
-                         const BwdParams* p, int warps, cudaStream_t s) {
+                         const BwdParams* p, int warps, int* dev_err, cudaStream_t s) {
     const int blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     bwd_dkdv_simt_kernel<D><<<blocks, kWarpsPerBlock * 32, 0, s>>>(
         static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
-        static_cast<const float*>(dout), *p);
+        static_cast<const float*>(dout), *p, dev_err);
     return cudaGetLastError();
   }
 };
@@ -239,9 +253,9 @@ int attn_bwd_simt_warps(const BwdItem& it, int heads) { return it.stat.len * hea
 // p.cta_start holds warp offsets here.
 cudaError_t launch_attn_bwd_simt(bool dkdv, const void* q, const void* k, const void* v,
                                  const void* dout, const BwdParams& p, int D, int warps,
-                                 cudaStream_t s) {
-  return dkdv ? dispatch_d<RunDkdv>(D, q, k, v, dout, &p, warps, s)
-              : dispatch_d<RunDq>(D, q, k, v, dout, &p, warps, s);
+                                 int* dev_err, cudaStream_t s) {
+  return dkdv ? dispatch_d<RunDkdv>(D, q, k, v, dout, &p, warps, dev_err, s)
+              : dispatch_d<RunDq>(D, q, k, v, dout, &p, warps, dev_err, s);
 }
 
 cudaError_t launch_bwd_delta_f32(const void* out, const void* dout, float* delta, int64_t rows,

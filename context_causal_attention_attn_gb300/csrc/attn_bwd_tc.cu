@@ -285,6 +285,19 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   const int nstr = kDKDV ? nper * grp : nper;
   const int kvh = kDKDV ? shead : shead / grp;
   const int64_t stride = kStriped ? p.stride : 1;
+  // Bounds-checked build: the stationary tile's rows (which are also its
+  // gradient rows and, for dQ, its lse / delta columns) lie inside their
+  // tensors; a tile that fails is recorded and skips its global reads and
+  // writes.
+  bool in_bounds = true;
+  if (kDebugBounds) {
+    const int64_t t0 = it.stat.stripe + stride * srow0;
+    const int64_t t1 = it.stat.stripe + stride * (srow0 + nstat - 1);
+    in_bounds = nstat > 0 && srow0 >= 0 && it.stat.stripe >= 0 && it.stat.stripe < stride &&
+                t1 < (kDKDV ? p.k_rows : p.q_rows) && shead < (kDKDV ? p.Hkv : p.H) &&
+                (kDKDV || t1 < p.ld) && t0 >= 0;
+    if (threadIdx.x == 0) bounds_ok(in_bounds, dev_err, kSiteBwdStat);
+  }
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -361,6 +374,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         int64_t row, pos;
         int n, stripe, qh;
         str_tile(pc, row, pos, n, stripe, qh);
+        // (a copy outside the tensor would only read the fill value)
+        if (kDebugBounds)
+          bounds_ok(n > 0 && row >= 0 && stripe >= 0 && stripe < stride &&
+                        stripe + stride * (row + n - 1) < (kDKDV ? p.q_rows : p.k_rows) &&
+                        qh < p.H,
+                    dev_err, kSiteBwdStr);
         bool ok = true;
         for (int w = 0; w < 2; ++w) {
           const int st = slot_of(j, w);
@@ -512,7 +531,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     float my_dl = 0.f;
     if (!kDKDV) {
       float l = -CUDART_INF_F;
-      if (row < nstat) {
+      if (row < nstat && in_bounds) {
         const float v = p.lse[static_cast<int64_t>(shead) * p.ld + my_tok];
         l = v == -CUDART_INF_F ? -CUDART_INF_F : -v * LOG2E;
         my_dl = p.delta[static_cast<int64_t>(shead) * p.ld + my_tok];
@@ -543,6 +562,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       str_tile(lc, trow, tpos, tn, tstripe, qh);
       if (ccol >= tn) return is_l ? CUDART_INF_F : 0.f;
       const int64_t tok = tstripe + stride * (trow + ccol);
+      if (kDebugBounds && !bounds_ok(tok >= 0 && tok < p.ld && qh < p.H, dev_err, kSiteBwdStr))
+        return is_l ? CUDART_INF_F : 0.f;
       return (is_l ? p.lse : p.delta)[static_cast<int64_t>(qh) * p.ld + tok];
     };
     float col_next = (kDKDV && nstr > 0) ? col_load() : 0.f;
@@ -678,7 +699,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const bool accumulate = (it.flags & kBwdAccumulate) != 0;
     const bool final_out = (it.flags & kBwdFinal) != 0;
     const int nheads = kDKDV ? p.Hkv : p.H;
-    if (ok) {
+    if (ok && in_bounds) {
       // The accumulators pass through shared memory (the streamed rings,
       // idle once every MMA is done) so that global memory is read and
       // written 256 bytes of a row per half-warp instruction; thread = row

@@ -20,7 +20,7 @@ constexpr int kSimtRows = 128;  // query rows per block (one head)
 
 template <int D>
 __global__ void __launch_bounds__(kSimtRows)
-    attn_fwd_simt_kernel(const __grid_constant__ AttnParams p) {
+    attn_fwd_simt_kernel(const __grid_constant__ AttnParams p, int* dev_err) {
   int ii = 0;
   while (ii + 1 < p.nitems && static_cast<int>(blockIdx.x) >= p.cta_start[ii + 1]) ++ii;
   const WorkItem& it = p.items[ii];
@@ -38,6 +38,19 @@ __global__ void __launch_bounds__(kSimtRows)
 
   const int64_t qrow_i = it.q_mem_row + static_cast<int64_t>(b) * it.b_q_rows + row;
   const int64_t qtok = it.q_stripe + static_cast<int64_t>(p.stripe) * qrow_i;
+  if (kDebugBounds) {
+    // the row of q, of out / acc (out has the rows of q) and of lse
+    const int64_t orow = it.o_row + static_cast<int64_t>(b) * it.b_o_rows +
+                         static_cast<int64_t>(row) * it.o_stride;
+    const int64_t lcol = it.lse_col + static_cast<int64_t>(row) * it.o_stride;
+    const int64_t lh = static_cast<int64_t>(head) + static_cast<int64_t>(b) * it.b_lse_heads;
+    if (!bounds_ok(qrow_i >= 0 && qrow_i < p.q_rows / p.stripe && it.q_stripe >= 0 &&
+                       it.q_stripe < p.stripe && kvh >= 0 && kvh < p.Hkv && orow >= 0 &&
+                       orow < p.q_rows && lcol >= 0 && lcol < p.ld_lse &&
+                       lh < static_cast<int64_t>(p.H) * it.batch,
+                   dev_err, kSiteFwdSimt))
+      return;
+  }
   const float* qrow =
       static_cast<const float*>(p.q) + (qtok * p.H + head) * static_cast<int64_t>(D);
   float q[D];
@@ -66,6 +79,11 @@ __global__ void __launch_bounds__(kSimtRows)
       if (vis < n) n = static_cast<int>(vis);
     }
     for (int j = 0; j < n; ++j) {
+      if (kDebugBounds && !bounds_ok(sg.mem_row + kb + j >= 0 &&
+                                         sg.mem_row + kb + j < p.k_rows / p.kv_stripe &&
+                                         sg.stripe >= 0 && sg.stripe < p.kv_stripe,
+                                     dev_err, kSiteFwdSimt))
+        break;
       const int64_t ktok = sg.stripe + static_cast<int64_t>(p.kv_stripe) * (sg.mem_row + kb + j);
       const int64_t off = (ktok * p.Hkv + kvh) * static_cast<int64_t>(D);
       const float* kr = K + off;
@@ -151,12 +169,12 @@ __global__ void __launch_bounds__(kSimtRows)
   *lse_ptr = lse_new;
 }
 
-cudaError_t launch_attn_simt(const AttnParams& p, int ctas, cudaStream_t stream) {
+cudaError_t launch_attn_simt(const AttnParams& p, int ctas, int* dev_err, cudaStream_t stream) {
   switch (p.D) {
-    case 16: attn_fwd_simt_kernel<16><<<ctas, kSimtRows, 0, stream>>>(p); break;
-    case 32: attn_fwd_simt_kernel<32><<<ctas, kSimtRows, 0, stream>>>(p); break;
-    case 64: attn_fwd_simt_kernel<64><<<ctas, kSimtRows, 0, stream>>>(p); break;
-    case 128: attn_fwd_simt_kernel<128><<<ctas, kSimtRows, 0, stream>>>(p); break;
+    case 16: attn_fwd_simt_kernel<16><<<ctas, kSimtRows, 0, stream>>>(p, dev_err); break;
+    case 32: attn_fwd_simt_kernel<32><<<ctas, kSimtRows, 0, stream>>>(p, dev_err); break;
+    case 64: attn_fwd_simt_kernel<64><<<ctas, kSimtRows, 0, stream>>>(p, dev_err); break;
+    case 128: attn_fwd_simt_kernel<128><<<ctas, kSimtRows, 0, stream>>>(p, dev_err); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -158,6 +158,23 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
   const int n_a = visible_tiles(it, p, q_pos0 + nrows_a - 1, causal);
   const int n_b = nrows_b > 0 ? visible_tiles(it, p, q_pos0 + tc::BM + nrows_b - 1, causal) : 0;
   const int nkv = max(n_a, n_b);
+  // Bounds-checked build: the tile's q rows, out / acc rows and lse columns
+  // lie inside their tensors (out has the rows of q); a tile that fails is
+  // recorded and skips its global reads and writes.
+  bool in_bounds = true;
+  if (kDebugBounds) {
+    const int nr = nrows_a + nrows_b;
+    const int64_t os = kStriped ? it.o_stride : 1;
+    const int64_t o0 =
+        it.o_row + static_cast<int64_t>(b) * it.b_o_rows + static_cast<int64_t>(row0) * os;
+    const int64_t c0 = it.lse_col + static_cast<int64_t>(row0) * os;
+    const int64_t lh = static_cast<int64_t>(head) + static_cast<int64_t>(b) * it.b_lse_heads;
+    in_bounds = nr > 0 && q_mem0 >= 0 && q_mem0 + nr <= p.q_rows / p.stripe &&
+                it.q_stripe >= 0 && it.q_stripe < p.stripe && kvh >= 0 && kvh < p.Hkv &&
+                o0 >= 0 && o0 + (nr - 1) * os < p.q_rows && lh < static_cast<int64_t>(p.H) * it.batch &&
+                c0 >= 0 && c0 + (nr - 1) * os < p.ld_lse;
+    if (threadIdx.x == 0) bounds_ok(in_bounds, dev_err, kSiteFwdTile);
+  }
 
   // ---------------------------------------------------------------- setup
   // The producer thread initialises the barriers and starts the Q and first
@@ -176,6 +193,11 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
     pcur.next(it, p, q_pos0 + nrows_a - 1, causal);
     if (!kStriped) kstripe = 0;
     const int krow = static_cast<int>(kmem + k_boff);
+    // (a copy outside the tensor would only read the fill value)
+    if (kDebugBounds)
+      bounds_ok(kmem + k_boff >= 0 && kmem + k_boff + nk <= p.k_rows / p.kv_stripe &&
+                    kstripe >= 0 && kstripe < p.kv_stripe,
+                dev_err, kSiteFwdKV);
     for (int w = 0; w < 2; ++w) {
       const int n = 2 * j + w;
       const int st = n % C::STAGES;
@@ -267,9 +289,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         }
       };
       // tile 0 was issued before the sync
-      if (merge && nkv > 0 && prefetch_at == 0) prefetch_acc();
+      if (merge && in_bounds && nkv > 0 && prefetch_at == 0) prefetch_acc();
       for (int j = 1; j < nkv; ++j) {
-        if (merge && j == prefetch_at) prefetch_acc();
+        if (merge && in_bounds && j == prefetch_at) prefetch_acc();
         if (!issue_kv(j)) break;
       }
       // let every copy this thread issued land before the CTA can exit
@@ -503,7 +525,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
 
       // ---------------------------------------------------- epilogue
       // the last S is done (Q and K/V stage 0 are free) while the last PV runs
-      if (ok && merge && nx > 0) fetch_acc();
+      if (ok && in_bounds && merge && nx > 0) fetch_acc();
       bool have_o = ok && nx > 0;
       if (have_o) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(bar(C::BAR_O_DONE + x), (nx - 1) & 1,
@@ -521,7 +543,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
       if (ok && nx == 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::BAR_Q), 0, tc::WAIT_LIMIT_NS, abort_flag));
         if (!ok) record_timeout(dev_err, abort_flag);
-        if (ok && merge) fetch_acc();
+        if (ok && in_bounds && merge) fetch_acc();
       }
       // out, acc and lse rows may be touched by the grid launched before
       // this one (a merge's fetch waited already; waiting again returns at
@@ -529,7 +551,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
       grid_wait_prerequisites();
       cp_async_wait_all();
       __syncwarp();
-      const bool valid = ok && row < nrows;
+      const bool valid = ok && in_bounds && row < nrows;
       const float* lse_stg = reinterpret_cast<const float*>(smem + C::OFF_LSE);
       const float LOG2E = 1.4426950408889634f;
       const float LN2 = 0.6931471805599453f;
@@ -553,7 +575,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         }
       }
       const float c_blk = l != 0.f ? w_blk / l : 0.f;
-      if (ok) {
+      if (ok && in_bounds) {
         float* stg = reinterpret_cast<float*>(smem + C::OFF_Q);
         const int wrow0 = quad * 32;                // this warp's rows
         const int nwrows = min(32, nrows - wrow0);  // of them inside the tile

@@ -118,6 +118,35 @@ struct AttnParams {
 // Status word written by kernels whose bounded wait expired.
 constexpr int kDevErrTimeout = 1;
 
+// Bounds-checked build (compiled with CP_DEBUG_BOUNDS, as libcpattn_debug.so):
+// the kernels check that every tile or row they read or write lies inside
+// its tensor; a failed check writes kDevErrBounds | site << 8 to the status
+// word and the access is skipped.  Release builds compile the checks away.
+constexpr int kDevErrBounds = 2;
+enum BoundsSite : int {
+  kSiteFwdTile = 1,  // tensor-core forward: a query tile's q rows, out / acc rows, lse columns
+  kSiteFwdKV = 2,    // tensor-core forward: a K/V tile's rows
+  kSiteFwdSimt = 3,  // CUDA-core forward: a query row or a key row
+  kSiteBwdStat = 4,  // tensor-core backward: a stationary tile's rows and lse / delta columns
+  kSiteBwdStr = 5,   // tensor-core backward: a streamed tile's rows or lse / delta columns
+  kSiteBwdSimt = 6,  // CUDA-core backward: a stationary or streamed row
+};
+#ifdef CP_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+#ifdef __CUDACC__
+// `cond` in the bounds-checked build, recording `site` when it fails; always
+// true (and compiled away) in release builds.
+__device__ __forceinline__ bool bounds_ok(bool cond, int* dev_err, int site) {
+  if (!kDebugBounds) return true;
+  if (!cond) atomicCAS(dev_err, 0, kDevErrBounds | (site << 8));
+  return cond;
+}
+#endif
+
 }  // namespace cpattn
 
 namespace cpattn {
@@ -169,6 +198,7 @@ struct BwdParams {
   int cta_start[kMaxItems + 1];
   BwdItem items[kMaxItems];
   int64_t ring_C, ring_S;  // chunk rows and sequence length of chunk-list items
+  int64_t q_rows, k_rows;  // rows of the q / dout / dq and k / v / dk / dv tensors (bounds)
 };
 
 }  // namespace cpattn

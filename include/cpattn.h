@@ -53,7 +53,8 @@ typedef enum {
   CP_ERR_DTYPE = -3,   /* unsupported dtype combination                        */
   CP_ERR_ALIGN = -4,   /* a pointer is not 16-byte aligned                     */
   CP_ERR_CUDA = -5,    /* a CUDA runtime/driver call failed                    */
-  CP_ERR_TIMEOUT = -6  /* a device-side bounded wait expired (see below)       */
+  CP_ERR_TIMEOUT = -6, /* a device-side bounded wait expired (see below)       */
+  CP_ERR_BOUNDS = -7   /* bounds-checked build: a kernel's bounds check failed  */
 } cp_status;
 
 typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
@@ -546,10 +547,24 @@ int cp_ring_backward_host(const void* hq, const void* hk, const void* hv, const 
  * cp_check_device_error - synchronise `stream`, then report and clear the
  * device status word: CP_OK, or CP_ERR_TIMEOUT if a kernel's bounded wait
  * expired since the last check (the kernel then skipped the rest of its
- * work and its outputs are undefined), or CP_ERR_CUDA if the
- * synchronisation failed.
+ * work and its outputs are undefined), CP_ERR_BOUNDS (bounds-checked build
+ * only) if a kernel found a tile or row outside its tensor (it skipped
+ * those reads and writes; the message names the check), or CP_ERR_CUDA if
+ * the synchronisation failed.  The first error since the last check wins.
  */
 int cp_check_device_error(cp_stream_t stream);
+
+/*
+ * cp_debug_bounds - 1 in the bounds-checked build of the library
+ * (libcpattn_debug.so, compiled with CP_DEBUG_BOUNDS), 0 in the release
+ * build (libcpattn.so).  In the bounds-checked build every attention kernel
+ * (forward and backward, tensor-core and fp32) checks, per tile or row,
+ * that what it reads and writes of q, k, v, out / acc, lse, delta and the
+ * gradients lies inside the tensors the call describes, records a failure
+ * in the device status word (see cp_check_device_error) and skips the
+ * access.  Results are otherwise bit-identical to the release build.
+ */
+int cp_debug_bounds(void);
 
 /*
  * cp_selftest_wait_timeout - failure-detection self-test: launches one

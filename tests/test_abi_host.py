@@ -46,6 +46,23 @@ def test_version(cp):
     assert "sm_103a" in cp.cp_version()
 
 
+def test_release_build_is_not_bounds_checked(cp):
+    from context_causal_attention_attn_gb300 import build
+    assert ctypes.CDLL(build.LIB).cp_debug_bounds() == 0
+
+
+def test_bounds_checked_build_exports_every_declared_symbol():
+    """The bounds-checked variant (sources compiled with CP_DEBUG_BOUNDS)
+    compiles, links, exports the same boundary and reports that it checks."""
+    from context_causal_attention_attn_gb300 import build
+    path = build.build(debug=True)
+    assert path == build.LIB_DEBUG != build.LIB
+    lib = ctypes.CDLL(path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert lib.cp_debug_bounds() == 1
+
+
 @pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
 @pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16])
 def test_ring_schedule_matches_oracle(cp, layout, P):
