@@ -116,19 +116,30 @@ def load_peaks():
             "fallback"
 
 
+FWD_KERNEL_SOURCES = ("attn_tc.cu", "attn_fwd_common.cuh", "sm100.cuh", "internal.h")
+
+
+def forward_kernel_sha():
+    """Digest of the sources the forward attention kernel is compiled from."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in FWD_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "context_causal_attention_attn_gb300", "csrc", name),
+                  "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(workload):
     """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, or None when absent or taken on another kernel source."""
+    summary, or None when absent or taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "attn_fwd_tc_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    import hashlib
-    src = os.path.join(ROOT, "context_causal_attention_attn_gb300", "csrc", "attn_tc.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if d.get("kernel_sha") != sha:
+    if d.get("kernel_sha") != forward_kernel_sha():
         return None
     return d.get("per_launch_bytes", {}).get(workload)
 
@@ -513,7 +524,7 @@ def run_gpu(args, wl, rank, world, local):
         h_.copy_(d_)
     h2d_gbs, d2h_gbs, link_bytes, link_spread = link_gbs(q, hq, stream)
     q.copy_(hq)
-    K_e2e = max(1, min(K, 3))
+    K_e2e = max(1, min(K, 5))
     host_api = wl["kind"] in ("ring", "ring_steps", "ulysses", "usp")
     host_fn = {"ulysses": "cp_ulysses_forward_host", "usp": "cp_usp_forward_host"}.get(
         wl["kind"], "cp_ring_forward_host")
@@ -793,7 +804,7 @@ def run_bwd(args, wl, rank, world, local):
     for h_, d_ in zip(host_in, src):
         h_.copy_(d_)
     h2d_gbs, d2h_gbs, link_bytes, link_spread = link_gbs(dq, host_out[0], stream)
-    K_e2e = max(1, min(K, 3))
+    K_e2e = max(1, min(K, 5))
     host_api = not train
     if host_api:
         # the C ABI's host-buffer entry point: copies in, ring backward, copies
@@ -972,7 +983,7 @@ def run_hbm(args, wl, rank, world, local):
         h_.copy_(d_)
     h2d_gbs, d2h_gbs, _, link_spread = link_gbs(inputs[0], hin[0], stream)
     inputs[0].copy_(hin[0])
-    K_e2e = max(1, min(K, 3))
+    K_e2e = max(1, min(K, 5))
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
