@@ -149,6 +149,7 @@ int launch_items(Launch& L, cp_dtype in_dt, const void* q, int64_t q_rows, const
   }
   p.tile_start[p.nitems] = static_cast<int>(tiles);
   if (p.head_major) {
+    if (p.hm_long < 0 || p.hm_long > tiles) p.hm_long = static_cast<int>(tiles);
     // the grid is tiles x (heads x batch): every item has the same batch
     bool uniform = in_dt == CP_BF16;
     for (int i = 1; i < p.nitems; ++i) uniform = uniform && p.items[i].batch == p.items[0].batch;
@@ -402,6 +403,52 @@ int ring_step_impl(const void* q, const void* k, const void* v, cp_dtype in_dt, 
   return launch_items(L, in_dt, q, q_rows, kk, vv, k_rows, stream, dependent);
 }
 
+// Head-major grid of the one-launch ring: how many of each head's tile ranks
+// (the items in order, later query tiles first -- roughly longest first)
+// run head by head before the rest runs rank by rank across the nh heads
+// (heads x batch).  Run purely head by head, the grid ends with the last
+// head's tiles: its longest CTA (Lmax KV tiles) starts about T_h = (the
+// head's KV tiles) / (resident CTAs) before the other CTAs run out of work,
+// so the launch ends on a tail of Lmax - T_h with most SMs idle (at 32K: 256
+// against 108 tiles, 3.5% of the launch; none at 128K).  The shortest
+// ranks of every head, together holding the work of that tail on every
+// resident CTA, are moved to the end and run across the heads.
+int head_major_lead(const std::vector<WorkItem>& items, int64_t C, int64_t S, int nh, int dev) {
+  auto chunk_rows = [&](int64_t c) -> int64_t {
+    return std::max<int64_t>(0, std::min<int64_t>(S, (c + 1) * C) - c * C);
+  };
+  std::vector<int64_t> w;  // KV tiles of each tile rank of one head
+  for (const WorkItem& it : items) {
+    const int nt = (it.sq + 127) / 128;
+    for (int k = 0; k < nt; ++k) {
+      const int t = nt - 1 - k;
+      const int64_t qp_last = it.q_pos + std::min<int64_t>(it.sq, (t + 1) * 128) - 1;
+      int64_t n = 0;
+      for (int c = 0; c < it.nchunk; ++c) {
+        const int64_t pos = it.chunk[c] * C, len = chunk_rows(it.chunk[c]);
+        const int64_t vis = std::max<int64_t>(0, std::min<int64_t>(len, qp_last - pos + 1));
+        n += (vis + 127) / 128;
+      }
+      w.push_back(n);
+    }
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+  const int64_t slots = 2 * static_cast<int64_t>(std::max(sms, 1));  // two CTAs per SM
+  int64_t total = 0, lmax = 0;
+  for (int64_t x : w) {
+    total += x;
+    lmax = std::max(lmax, x);
+  }
+  const int64_t tail = lmax - total / slots;  // KV tiles of one CTA
+  if (tail <= 0 || nh < 1) return static_cast<int>(w.size());
+  const int64_t need = (tail * slots + nh - 1) / nh;  // per head
+  int64_t got = 0;
+  size_t lead = w.size();
+  while (lead > 0 && got < need) got += w[--lead];
+  return static_cast<int>(lead);
+}
+
 // The ring in one launch (bf16 inputs, contiguous or zigzag layout): one
 // work item per (virtual rank r, own query chunk qc), whose key segments are
 // the chunks rank r holds at steps t = 0, 1, ..., P-1 (src = (r - t) mod P,
@@ -431,16 +478,16 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
     L.p.kv_group = rb->kv_group;
   }
   // Every query tile walks its head's whole visible K/V.  When all heads' K/V
-  // is more than half of L2, run the grid head by head so that the CTAs
-  // resident at one time share one head's K/V (at 32K this cut DRAM reads
-  // from 4.8 GB to 0.83 GB per launch); otherwise keep the items'
-  // longest-first order across all heads, which ends with a shorter tail
-  // (4K: 954 against 767 TFLOP/s head by head).
+  // is more than L2 holds, run the grid head by head so that the CTAs
+  // resident at one time share one head's K/V (at 32K, 512 MiB of K/V, this
+  // cut DRAM reads from 4.8 GB to 0.83 GB per launch); otherwise keep the
+  // items' longest-first order across all heads, which ends with a shorter
+  // tail (4K, 64 MiB of K/V: 954 against 767 TFLOP/s head by head).
   int dev = 0, l2 = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
     l2 = 0;
-  L.p.head_major = k_rows * Hkv * static_cast<int64_t>(D) * 2 * 2 > static_cast<int64_t>(l2) / 2;
+  L.p.head_major = k_rows * Hkv * static_cast<int64_t>(D) * 2 * 2 > static_cast<int64_t>(l2);
   std::vector<int64_t> work;  // visible keys x rows, for the longest-first order
   for (int r = 0; r < P; ++r) {
     int qcs[2];
@@ -487,6 +534,7 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
   std::vector<WorkItem> sorted;
   for (size_t i : order) sorted.push_back(L.items[i]);
   L.items.swap(sorted);
+  if (L.p.head_major) L.p.hm_long = head_major_lead(L.items, C, S, H * (rb ? rb->batch : 1), dev);
   return launch_items(L, CP_BF16, q, q_rows, k, v, k_rows, stream);
 }
 

@@ -126,10 +126,21 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
   int ii = 0, pair, local;
   const WorkItem* itp;
   if (p.head_major) {
-    // head by head; within a head the items in order, later query tiles first
+    // tile rank r of a head: the items in order, later query tiles first.
+    // Ranks [0, hm_long) head by head, then the rest rank by rank across
+    // the heads (the grid is tiles x heads x batch CTAs).
     const int tiles = p.tile_start[p.nitems];
-    const int r = static_cast<int>(blockIdx.x) % tiles;
-    local = static_cast<int>(blockIdx.x) / tiles;
+    const int nh = static_cast<int>(gridDim.x) / tiles;
+    const int lead = p.hm_long * nh;
+    const int g = static_cast<int>(blockIdx.x);
+    int r;
+    if (g < lead) {
+      r = g % p.hm_long;
+      local = g / p.hm_long;
+    } else {
+      r = p.hm_long + (g - lead) / nh;
+      local = (g - lead) % nh;
+    }
     while (ii + 1 < p.nitems && r >= p.tile_start[ii + 1]) ++ii;
     itp = &p.items[ii];
     const int npairs = (itp->sq + NT * tc::BM - 1) / (NT * tc::BM);
@@ -575,7 +586,59 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         }
       }
       const float c_blk = l != 0.f ? w_blk / l : 0.f;
-      if (ok && in_bounds) {
+      if (ok && in_bounds && final_out && p.out_dt == 1 && !merge) {
+        // A bf16 result with nothing to merge: rows of 256 bytes staged in
+        // bf16 over the Q buffer (16-byte chunk c of row r at c ^ (r & 7)),
+        // half the shared-memory traffic of the fp32 staging below, which
+        // the other CTA's MMAs on this SM compete for.
+        uint4* stg16 = reinterpret_cast<uint4*>(smem + C::OFF_Q);
+        uint4* srow16 = stg16 + row * 16;
+        const int wrow0 = quad * 32;                // this warp's rows
+        const int nwrows = min(32, nrows - wrow0);  // of them inside the tile
+        const int sw = row & 7;
+#pragma unroll 1
+        for (int h4 = 0; h4 < 4; ++h4) {
+          uint32_t o[32];
+          __syncwarp();
+          if (have_o) {
+            tmem_ld32(t_o + h4 * 32, o);
+            tmem_wait_ld();
+            reg_dep(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            auto pk = [&](int e) {
+              return pack_bf16x2(__uint_as_float(o[8 * i + e]) * c_blk,
+                                 __uint_as_float(o[8 * i + e + 1]) * c_blk);
+            };
+            srow16[(h4 * 4 + i) ^ sw] = make_uint4(pk(0), pk(2), pk(4), pk(6));
+          }
+        }
+        __syncwarp();
+        // two rows per warp instruction (16 lanes x 16 bytes each), eight
+        // instructions' shared-memory reads ahead of their stores
+        const int sub = lane >> 4, l16 = lane & 15;
+        __nv_bfloat16* dst16 = reinterpret_cast<__nv_bfloat16*>(p.out);
+        const int64_t el0 = out_el0() + 8 * l16, stp = out_step();
+#pragma unroll 1
+        for (int i0 = 0; i0 < 32; i0 += 16) {
+          uint4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int rr = wrow0 + i0 + 2 * u + sub;
+            v[u] = stg16[rr * 16 + (l16 ^ (rr & 7))];
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int rr = i0 + 2 * u + sub;  // within this warp's rows
+            if (rr < nwrows)
+              *reinterpret_cast<uint4*>(dst16 + el0 + (wrow0 + rr) * stp) = v[u];
+          }
+        }
+      } else if (ok && in_bounds) {
         float* stg = reinterpret_cast<float*>(smem + C::OFF_Q);
         const int wrow0 = quad * 32;                // this warp's rows
         const int nwrows = min(32, nrows - wrow0);  // of them inside the tile

@@ -109,9 +109,13 @@ struct AttnParams {
   int64_t ring_C, ring_S;      // chunk rows and sequence length of chunk-list items
   // head_major: the grid runs head by head (all items' query tiles of head 0,
   // then head 1, ...), so the CTAs resident at one time read one head's K/V;
-  // tile_start is the prefix sum of query tiles per item.  Otherwise item by
-  // item (cta_start), query tiles fastest within a head.
+  // tile_start is the prefix sum of query tiles per item.  Only the tile
+  // ranks [0, hm_long) of every head run that way; the remaining (shortest)
+  // ranks follow, rank by rank across all heads, so that the grid ends on
+  // short tiles.  Otherwise item by item (cta_start), query tiles fastest
+  // within a head.
   int head_major;
+  int hm_long;
   int tile_start[kMaxItems + 1];
 };
 
