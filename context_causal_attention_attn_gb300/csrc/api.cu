@@ -510,6 +510,7 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
         w.b_lse_heads = rb->b_lse_heads;
       }
       w.flags = kFlagCausal | kFlagFinal;
+      w.q_chunk = qc;
       int64_t keys = 0;
       for (int t = 0; t < P; ++t) {
         const int src = ((r - t) % P + P) % P;
@@ -520,6 +521,7 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
           if (w.nchunk >= kMaxRingChunks) return fail(CP_ERR_ARG, "too many ring chunks");
           w.chunk[w.nchunk++] = static_cast<uint8_t>(kcs[b]);
           keys += kcs[b] == qc ? chunk_rows(qc) / 2 : chunk_rows(kcs[b]);
+          if (kcs[b] != qc) w.full_tiles += static_cast<int32_t>((chunk_rows(kcs[b]) + 127) / 128);
         }
       }
       L.items.push_back(w);

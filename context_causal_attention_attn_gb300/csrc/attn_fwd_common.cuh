@@ -100,6 +100,12 @@ struct TileCursor {
 // Number of KV tiles a query tile whose last row sits at qp_last evaluates.
 __device__ __forceinline__ int visible_tiles(const WorkItem& it, const AttnParams& p,
                                              int64_t qp_last, bool causal) {
+  if (it.nchunk > 0 && causal) {
+    // every chunk but the query chunk lies before it
+    const int64_t pos = static_cast<int64_t>(it.q_chunk) * p.ring_C;
+    const int len = static_cast<int>(min(p.ring_S - pos, p.ring_C));
+    return it.full_tiles + seg_visible_tiles(pos, len, qp_last, true);
+  }
   int n = 0;
   const int ns = item_nseg(it);
   for (int s = 0; s < ns; ++s) {
@@ -109,6 +115,22 @@ __device__ __forceinline__ int visible_tiles(const WorkItem& it, const AttnParam
     n += seg_visible_tiles(pos, len, qp_last, causal);
   }
   return n;
+}
+
+// The last index i < n with start[i] <= x (start ascending, start[0] <= x):
+// the item of grid position x.  A binary search: the kernel parameters sit
+// in the constant bank, where each dependent load of a linear search costs
+// a cache round trip.
+__device__ __forceinline__ int last_at_most(const int* start, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (start[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
 
 __device__ __forceinline__ void record_timeout(int* dev_err, volatile int* abort_flag) {

@@ -141,12 +141,12 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
       r = p.hm_long + (g - lead) / nh;
       local = (g - lead) % nh;
     }
-    while (ii + 1 < p.nitems && r >= p.tile_start[ii + 1]) ++ii;
+    ii = last_at_most(p.tile_start, p.nitems, r);
     itp = &p.items[ii];
     const int npairs = (itp->sq + NT * tc::BM - 1) / (NT * tc::BM);
     pair = npairs - 1 - (r - p.tile_start[ii]);
   } else {
-    while (ii + 1 < p.nitems && static_cast<int>(blockIdx.x) >= p.cta_start[ii + 1]) ++ii;
+    ii = last_at_most(p.cta_start, p.nitems, static_cast<int>(blockIdx.x));
     itp = &p.items[ii];
     local = static_cast<int>(blockIdx.x) - p.cta_start[ii];
     const int npairs = (itp->sq + NT * tc::BM - 1) / (NT * tc::BM);

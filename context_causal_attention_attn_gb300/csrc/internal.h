@@ -82,6 +82,11 @@ struct WorkItem {
   // C = AttnParams::ring_C, S = AttnParams::ring_S), and seg / nseg are unused.
   int32_t nchunk;
   uint8_t chunk[kMaxRingChunks];
+  // chunk-list items: the query chunk (which the list holds once) and the
+  // KV tiles of the list's other chunks, all earlier and so visible to
+  // every query row -- a query tile's visible tiles without a walk
+  int32_t q_chunk;
+  int32_t full_tiles;
 };
 
 struct AttnParams {
