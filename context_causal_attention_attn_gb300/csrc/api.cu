@@ -17,8 +17,8 @@
 
 namespace cpattn {
 cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const AttnParams& p, int ctas, int* dev_err, cudaStream_t stream,
-                           bool dependent);
+                           const CUtensorMap& to, const AttnParams& p, int ctas, int* dev_err,
+                           cudaStream_t stream, bool dependent);
 int attn_tc_ctas(const WorkItem& it, int H);
 cudaError_t launch_attn_simt(const AttnParams& p, int ctas, int* dev_err, cudaStream_t stream);
 int attn_simt_ctas(const WorkItem& it, int H);
@@ -176,10 +176,18 @@ int launch_items(Launch& L, cp_dtype in_dt, const void* q, int64_t q_rows, const
     int rc = make_map(&tq, q, q_rows, p.H, p.stripe, p.maps4d);
     if (rc == CP_OK) rc = make_map(&tk, k, k_rows, p.Hkv, p.kv_stripe, p.maps4d);
     if (rc == CP_OK) rc = make_map(&tv, v, k_rows, p.Hkv, p.kv_stripe, p.maps4d);
+    // a bf16 out [q_rows, H, D] with plain rows is written by TMA stores
+    // (whole tiles of unmerged results); otherwise the map is not used
+    CUtensorMap to = tq;
+    p.tma_out = 0;
+    if (rc == CP_OK && !p.maps4d && p.out_dt == 1 && p.out != nullptr) {
+      rc = make_map(&to, p.out, q_rows, p.H, 1, false);
+      p.tma_out = 1;
+    }
     if (rc != CP_OK) return rc;
     int* st = device_status_ptr();
     if (st == nullptr) return fail(CP_ERR_CUDA, "device status word unavailable");
-    e = launch_attn_tc(tq, tk, tv, p, static_cast<int>(total), st, stream, dependent);
+    e = launch_attn_tc(tq, tk, tv, to, p, static_cast<int>(total), st, stream, dependent);
   } else {
     int* st = device_status_ptr();
     if (st == nullptr) return fail(CP_ERR_CUDA, "device status word unavailable");

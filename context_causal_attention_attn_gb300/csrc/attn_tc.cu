@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o,
                        const __grid_constant__ AttnParams p, int* dev_err) {
   using C = tc::Cfg<NT>;
   // The staged epilogue reuses the Q and K/V buffers, which with two tiles
@@ -586,7 +587,47 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         }
       }
       const float c_blk = l != 0.f ? w_blk / l : 0.f;
-      if (ok && in_bounds && final_out && p.out_dt == 1 && !merge) {
+      if (!kStriped && p.tma_out && final_out && !merge && nrows == tc::BM && in_bounds) {
+        // A whole tile of bf16 result with nothing to merge: the rows are
+        // staged in the output map's two boxes (64 columns, 128-byte
+        // swizzle: 16-byte chunk j of row r at j ^ (r & 7)) and one thread
+        // stores them with two TMA copies.  Every softmax thread takes this
+        // branch (its condition is the CTA's), so all 128 reach the barrier.
+        uint4* box = reinterpret_cast<uint4*>(smem + C::OFF_Q);
+        const int sw = row & 7;
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2 && ok; ++h2) {
+          uint32_t o[2][32];
+          __syncwarp();
+          if (have_o) {
+            tmem_ld32(t_o + h2 * 64, o[0]);
+            tmem_ld32(t_o + h2 * 64 + 32, o[1]);
+            tmem_wait_ld();
+            reg_dep(o[0]);
+            reg_dep(o[1]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[0][i] = o[1][i] = 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            auto pk = [&](int e) {
+              return pack_bf16x2(__uint_as_float(o[i >> 2][8 * (i & 3) + e]) * c_blk,
+                                 __uint_as_float(o[i >> 2][8 * (i & 3) + e + 1]) * c_blk);
+            };
+            box[h2 * 1024 + row * 8 + (i ^ sw)] = make_uint4(pk(0), pk(2), pk(4), pk(6));
+          }
+        }
+        fence_proxy_async_smem();  // the staged rows, to the copy engine
+        named_bar_sync(1, 128);
+        if (row == 0 && *abort_flag == 0) {
+          const int orow0 = static_cast<int>(it.o_row + static_cast<int64_t>(b) * it.b_o_rows + row0);
+          tma_store_3d(&tm_o, sbase + C::OFF_Q, 0, head, orow0);
+          tma_store_3d(&tm_o, sbase + C::OFF_Q + 16384, 64, head, orow0);
+          bulk_commit_group();
+          bulk_wait_read_all();  // the boxes stay until the copies have read them
+        }
+      } else if (ok && in_bounds && final_out && p.out_dt == 1 && !merge) {
         // A bf16 result with nothing to merge: rows of 256 bytes staged in
         // bf16 over the Q buffer (16-byte chunk c of row r at c ^ (r & 7)),
         // half the shared-memory traffic of the fp32 staging below, which
@@ -596,25 +637,28 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         const int wrow0 = quad * 32;                // this warp's rows
         const int nwrows = min(32, nrows - wrow0);  // of them inside the tile
         const int sw = row & 7;
+        // 64 columns per TMEM round trip (two loads, one wait)
 #pragma unroll 1
-        for (int h4 = 0; h4 < 4; ++h4) {
-          uint32_t o[32];
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t o[2][32];
           __syncwarp();
           if (have_o) {
-            tmem_ld32(t_o + h4 * 32, o);
+            tmem_ld32(t_o + h2 * 64, o[0]);
+            tmem_ld32(t_o + h2 * 64 + 32, o[1]);
             tmem_wait_ld();
-            reg_dep(o);
+            reg_dep(o[0]);
+            reg_dep(o[1]);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
+            for (int i = 0; i < 32; ++i) o[0][i] = o[1][i] = 0u;
           }
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 8; ++i) {
             auto pk = [&](int e) {
-              return pack_bf16x2(__uint_as_float(o[8 * i + e]) * c_blk,
-                                 __uint_as_float(o[8 * i + e + 1]) * c_blk);
+              return pack_bf16x2(__uint_as_float(o[i >> 2][8 * (i & 3) + e]) * c_blk,
+                                 __uint_as_float(o[i >> 2][8 * (i & 3) + e + 1]) * c_blk);
             };
-            srow16[(h4 * 4 + i) ^ sw] = make_uint4(pk(0), pk(2), pk(4), pk(6));
+            srow16[(h2 * 8 + i) ^ sw] = make_uint4(pk(0), pk(2), pk(4), pk(6));
           }
         }
         __syncwarp();
@@ -723,8 +767,8 @@ static_assert(kNT == 1, "one query tile per CTA (two tiles per CTA measured slow
 int attn_tc_smem_bytes() { return static_cast<int>(tc::Cfg<kNT>::SMEM_BYTES); }
 
 cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const AttnParams& p, int ctas, int* dev_err, cudaStream_t stream,
-                           bool dependent) {
+                           const CUtensorMap& to, const AttnParams& p, int ctas, int* dev_err,
+                           cudaStream_t stream, bool dependent) {
   using C = tc::Cfg<kNT>;
   // the shared-memory attribute is a property of the function on each device
   static PerDeviceOnce attr_once;
@@ -753,8 +797,8 @@ cudaError_t launch_attn_tc(const CUtensorMap& tq, const CUtensorMap& tk, const C
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   if (p.maps4d)
-    return cudaLaunchKernelEx(&cfg, attn_fwd_tc_kernel<true, kNT>, tq, tk, tv, p, dev_err);
-  return cudaLaunchKernelEx(&cfg, attn_fwd_tc_kernel<false, kNT>, tq, tk, tv, p, dev_err);
+    return cudaLaunchKernelEx(&cfg, attn_fwd_tc_kernel<true, kNT>, tq, tk, tv, to, p, dev_err);
+  return cudaLaunchKernelEx(&cfg, attn_fwd_tc_kernel<false, kNT>, tq, tk, tv, to, p, dev_err);
 }
 
 // Number of CTAs one item occupies (kNT x 128 query rows per CTA).

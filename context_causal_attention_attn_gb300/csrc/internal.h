@@ -121,6 +121,7 @@ struct AttnParams {
   // within a head.
   int head_major;
   int hm_long;
+  int tma_out;                 // out has a TMA map (bf16 [q_rows, H, D], plain rows)
   int tile_start[kMaxItems + 1];
 };
 

@@ -96,6 +96,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Shared -> global copy of one box of a 3-D tensor map, in the calling
+// thread's bulk group (x = c0 a multiple of 16 bytes, coordinates >= 0).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until this thread's bulk groups have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Bring [addr, addr + bytes) into L2 without waiting (16-byte aligned
 // address, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* addr, uint32_t bytes) {
