@@ -776,7 +776,7 @@ def run_bwd(args, wl, rank, world, local):
         ("fwd", t) for t in range(P)]
     # the backward: cp_ring_backward's schedule (for bf16 contiguous / zigzag
     # one dK/dV and one dQ launch over every step, else one of each per step)
-    fused_bwd = cp.ring_runs_fused(q, layout)
+    fused_bwd = cp.ring_backward_runs_fused(q, layout)
     bstep = cp.cp_ring_backward_fused_step if fused_bwd else cp.cp_ring_backward_step
     nbl = 2 if fused_bwd else 2 * P
     launches = (fwd_launches if train else []) + [("delta", -1)] + [

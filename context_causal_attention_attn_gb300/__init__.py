@@ -15,7 +15,8 @@ from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_ERR_BOUNDS, CP_ERR_TIMEOUT, CP_F32
                    cp_ring_backward_host_workspace_size, cp_ring_backward_step,
                    cp_ring_backward_workspace_size, cp_ring_copy_workspace_size, cp_ring_forward,
                    cp_ring_forward_copy, cp_ring_forward_fused, cp_ring_forward_host,
-                   cp_ring_forward_steps, ring_runs_fused, cp_ring_backward_fused_step,
+                   cp_ring_forward_steps, ring_runs_fused, ring_backward_runs_fused,
+                   cp_ring_backward_fused_step,
                    cp_ring_forward_noalloc, cp_ring_host_workspace_size, cp_ring_step, cp_ring_step_blocks,
                    cp_ring_workspace_size, cp_selftest_wait_timeout, cp_seq_to_head,
                    cp_ulysses_forward, cp_ulysses_forward_host, cp_ulysses_host_workspace_size,
@@ -33,7 +34,8 @@ __all__ = [
     "cp_ring_backward_host_workspace_size", "cp_ring_backward_step",
     "cp_ring_backward_workspace_size", "cp_ring_copy_workspace_size", "cp_ring_forward",
     "cp_ring_forward_copy", "cp_ring_forward_fused", "cp_ring_forward_host",
-    "cp_ring_forward_steps", "ring_runs_fused", "cp_ring_backward_fused_step",
+    "cp_ring_forward_steps", "ring_runs_fused", "ring_backward_runs_fused",
+    "cp_ring_backward_fused_step",
     "cp_ring_forward_noalloc",
     "cp_ring_host_workspace_size", "cp_ring_step", "cp_ring_step_blocks",
     "cp_ring_workspace_size", "cp_selftest_wait_timeout", "cp_seq_to_head",

@@ -226,8 +226,14 @@ def _ring_buffers(q, out, out_dtype, lse, workspace):
 
 
 def ring_runs_fused(q, layout):
-    """Whether cp_ring_forward runs the ring in one launch (bf16 inputs,
-    contiguous or zigzag), which needs no workspace."""
+    """Whether cp_ring_forward runs the ring in one launch (bf16 inputs, any
+    layout), which needs no workspace."""
+    return q.dtype == torch.bfloat16 and layout in ("contiguous", "zigzag", "striped")
+
+
+def ring_backward_runs_fused(q, layout):
+    """Whether cp_ring_backward runs in two launches over all steps (bf16
+    inputs, contiguous or zigzag)."""
     return q.dtype == torch.bfloat16 and layout in ("contiguous", "zigzag")
 
 

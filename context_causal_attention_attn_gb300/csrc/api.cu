@@ -421,9 +421,10 @@ int ring_step_impl(const void* q, const void* k, const void* v, cp_dtype in_dt, 
 // against 108 tiles, 3.5% of the launch; none at 128K).  The shortest
 // ranks of every head, together holding the work of that tail on every
 // resident CTA, are moved to the end and run across the heads.
-int head_major_lead(const std::vector<WorkItem>& items, int64_t C, int64_t S, int nh, int dev) {
+int head_major_lead(const std::vector<WorkItem>& items, int64_t C, int64_t S, bool striped, int nh,
+                    int dev) {
   auto chunk_rows = [&](int64_t c) -> int64_t {
-    return std::max<int64_t>(0, std::min<int64_t>(S, (c + 1) * C) - c * C);
+    return striped ? C : std::max<int64_t>(0, std::min<int64_t>(S, (c + 1) * C) - c * C);
   };
   std::vector<int64_t> w;  // KV tiles of each tile rank of one head
   for (const WorkItem& it : items) {
@@ -433,7 +434,8 @@ int head_major_lead(const std::vector<WorkItem>& items, int64_t C, int64_t S, in
       const int64_t qp_last = it.q_pos + std::min<int64_t>(it.sq, (t + 1) * 128) - 1;
       int64_t n = 0;
       for (int c = 0; c < it.nchunk; ++c) {
-        const int64_t pos = it.chunk[c] * C, len = chunk_rows(it.chunk[c]);
+        const int64_t pos = striped ? (it.chunk[c] > it.q_stripe ? 1 : 0) : it.chunk[c] * C;
+        const int64_t len = chunk_rows(it.chunk[c]);
         const int64_t vis = std::max<int64_t>(0, std::min<int64_t>(len, qp_last - pos + 1));
         n += (vis + 127) / 128;
       }
@@ -471,8 +473,9 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
                     int D, int P, cp_layout layout, void* out, cp_dtype out_dt, float* lse,
                     cudaStream_t stream, const RingBatch* rb = nullptr) {
   const int64_t q_rows = rb ? rb->q_rows : S, k_rows = rb ? rb->k_rows : S;
+  const bool striped = layout == CP_STRIPED;
   const int64_t nchunks = layout == CP_ZIGZAG ? 2 * P : P;
-  const int64_t C = (S + nchunks - 1) / nchunks;
+  const int64_t C = (S + nchunks - 1) / nchunks;  // striped: S / P, the stripe length
   auto chunk_rows = [&](int64_t c) -> int64_t {
     return std::max<int64_t>(0, std::min<int64_t>(S, (c + 1) * C) - c * C);
   };
@@ -481,6 +484,13 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
               out_dt == CP_F32 ? static_cast<float*>(out) : nullptr, lse, S);
   L.p.ring_C = C;
   L.p.ring_S = S;
+  if (striped) {
+    // rank r's queries and every key it is handed are stripes (token
+    // r + P i), addressed through 4-D maps
+    L.p.stripe = P;
+    L.p.kv_stripe = P;
+    L.p.ring_striped = 1;
+  }
   if (rb) {
     L.p.b_q_heads = rb->b_q_heads;
     L.p.kv_group = rb->kv_group;
@@ -502,6 +512,30 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
     const int nq = rank_chunks(P, layout, r, qcs);
     for (int a = 0; a < nq; ++a) {
       const int qc = qcs[a];
+      if (striped) {
+        // stripe r against the stripes src = r, r-1, ... the steps hand it;
+        // every one holds keys visible to it (a causal prefix of each)
+        WorkItem w{};
+        w.q_stripe = r;
+        w.o_row = r;
+        w.o_stride = P;
+        w.lse_col = r;
+        w.sq = static_cast<int32_t>(C);
+        w.batch = 1;
+        if (rb) {
+          w.batch = rb->batch;
+          w.b_q_rows = rb->b_q_rows;
+          w.b_k_rows = rb->b_k_rows;
+          w.b_o_rows = rb->b_o_rows;
+          w.b_lse_heads = rb->b_lse_heads;
+        }
+        w.flags = kFlagCausal | kFlagFinal;
+        w.q_chunk = r;
+        for (int t = 0; t < P; ++t) w.chunk[w.nchunk++] = static_cast<uint8_t>(((r - t) % P + P) % P);
+        L.items.push_back(w);
+        work.push_back(C * C * P);  // alike for every rank
+        continue;
+      }
       if (chunk_rows(qc) == 0) continue;
       WorkItem w{};
       w.q_mem_row = qc * C;
@@ -544,7 +578,8 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
   std::vector<WorkItem> sorted;
   for (size_t i : order) sorted.push_back(L.items[i]);
   L.items.swap(sorted);
-  if (L.p.head_major) L.p.hm_long = head_major_lead(L.items, C, S, H * (rb ? rb->batch : 1), dev);
+  if (L.p.head_major)
+    L.p.hm_long = head_major_lead(L.items, C, S, striped, H * (rb ? rb->batch : 1), dev);
   return launch_items(L, CP_BF16, q, q_rows, k, v, k_rows, stream);
 }
 
@@ -942,9 +977,16 @@ namespace cpattn {
 // cp_last_error() of the calling thread.
 int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
 
-// Whether cp_ring_forward (and the host-buffer ring) run all steps in one
-// launch: bf16 inputs (tensor-core path) in the contiguous or zigzag layout.
+// Whether cp_ring_forward (and the host-buffer ring, Ulysses x ring) run all
+// steps in one launch: bf16 inputs (tensor-core path), any layout.
 bool ring_runs_fused(cp_dtype in_dt, cp_layout layout) {
+  return in_dt == CP_BF16 &&
+         (layout == CP_CONTIGUOUS || layout == CP_ZIGZAG || layout == CP_STRIPED);
+}
+
+// Whether cp_ring_backward runs in two launches over all steps: bf16 inputs
+// in the contiguous or zigzag layout.
+bool ring_bwd_runs_fused(cp_dtype in_dt, cp_layout layout) {
   return in_dt == CP_BF16 && (layout == CP_CONTIGUOUS || layout == CP_ZIGZAG);
 }
 }  // namespace cpattn
@@ -1061,8 +1103,6 @@ static int ring_fused_checked(const void* q, const void* k, const void* v, cp_dt
   if (rc != CP_OK) return rc;
   if (in_dt != CP_BF16)
     return fail(CP_ERR_DTYPE, "the one-launch ring needs bf16 inputs (tensor-core path)");
-  if (layout == CP_STRIPED)
-    return fail(CP_ERR_ARG, "the one-launch ring takes the contiguous or zigzag layout");
   if (!q || !k || !v || !out || !lse) return fail(CP_ERR_ARG, "null pointer argument");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(CP_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
@@ -1800,7 +1840,7 @@ static int ring_backward_launch(const void* q, const void* k, const void* v, con
   int rc = check_bwd_common(in_dt, H, Hkv, D, grad_dt);
   if (rc != CP_OK) return rc;
   if ((rc = check_ring(in_dt, S, H, Hkv, D, P, layout, grad_dt)) != CP_OK) return rc;
-  if (fused && !ring_runs_fused(in_dt, layout))
+  if (fused && !ring_bwd_runs_fused(in_dt, layout))
     return fail(in_dt != CP_BF16 ? CP_ERR_DTYPE : CP_ERR_ARG,
                 "the two-launch ring backward needs bf16 inputs and the contiguous or zigzag "
                 "layout");
@@ -1864,7 +1904,7 @@ int cp_ring_backward(const void* q, const void* k, const void* v, const void* ou
                      cp_dtype grad_dt, void* workspace, cp_stream_t stream) {
   // the tensor-core path runs the ring in two launches (every step inside
   // each), the rest one dK/dV and one dQ launch per step
-  const bool fused = ring_runs_fused(in_dt, layout);
+  const bool fused = ring_bwd_runs_fused(in_dt, layout);
   const int nl = fused ? 2 : 2 * P;
   for (int l = -1; l < nl; ++l) {
     const int rc = ring_backward_launch(q, k, v, out, dout, lse, in_dt, S, H, Hkv, D, P, layout,

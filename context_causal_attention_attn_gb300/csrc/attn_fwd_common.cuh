@@ -27,7 +27,15 @@ __device__ __forceinline__ int item_nseg(const WorkItem& it) {
 }
 __device__ __forceinline__ void item_seg(const WorkItem& it, const AttnParams& p, int s,
                                          int64_t& mem_row, int64_t& pos, int& len, int& stripe) {
-  if (it.nchunk > 0) {
+  if (it.nchunk > 0 && p.ring_striped) {
+    // stripe c in stripe indices; its keys trail the queries' by one
+    // position when c comes after the query stripe
+    const int c = it.chunk[s];
+    mem_row = 0;
+    pos = c > it.q_stripe ? 1 : 0;
+    len = static_cast<int>(p.ring_C);
+    stripe = c;
+  } else if (it.nchunk > 0) {
     const int64_t c0 = static_cast<int64_t>(it.chunk[s]) * p.ring_C;
     mem_row = c0;
     pos = c0;
@@ -100,7 +108,7 @@ struct TileCursor {
 // Number of KV tiles a query tile whose last row sits at qp_last evaluates.
 __device__ __forceinline__ int visible_tiles(const WorkItem& it, const AttnParams& p,
                                              int64_t qp_last, bool causal) {
-  if (it.nchunk > 0 && causal) {
+  if (it.nchunk > 0 && causal && !p.ring_striped) {
     // every chunk but the query chunk lies before it
     const int64_t pos = static_cast<int64_t>(it.q_chunk) * p.ring_C;
     const int len = static_cast<int>(min(p.ring_S - pos, p.ring_C));

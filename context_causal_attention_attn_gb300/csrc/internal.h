@@ -80,6 +80,9 @@ struct WorkItem {
   // the key segments are the sequence chunks chunk[0..nchunk) in the order
   // the ring's steps reach them (chunk c = rows [c C, min(S, (c+1) C)) with
   // C = AttnParams::ring_C, S = AttnParams::ring_S), and seg / nseg are unused.
+  // With AttnParams::ring_striped the chunks are stripes: chunk c is stripe
+  // c (C = S / P keys, stripe index i = token c + P i), whose key i is
+  // visible to query i' of stripe q_stripe when i + (c > q_stripe) <= i'.
   int32_t nchunk;
   uint8_t chunk[kMaxRingChunks];
   // chunk-list items: the query chunk (which the list holds once) and the
@@ -112,6 +115,7 @@ struct AttnParams {
   const void* v;
   int64_t q_rows, k_rows;      // rows of the q / k tensors (bounds)
   int64_t ring_C, ring_S;      // chunk rows and sequence length of chunk-list items
+  int ring_striped;            // chunk-list items name stripes (see WorkItem::chunk)
   // head_major: the grid runs head by head (all items' query tiles of head 0,
   // then head 1, ...), so the CTAs resident at one time read one head's K/V;
   // tile_start is the prefix sum of query tiles per item.  Only the tile

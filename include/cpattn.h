@@ -130,11 +130,10 @@ int64_t cp_ring_workspace_size(int64_t S, int H, int D, cp_dtype out_dt);
  *   chunk) pair in which some key precedes some query (for striped: every
  *   pair), merges the result into its running (out, lse) with the LSE merge,
  *   and skips the rest.
- *   Execution: with bf16 inputs in the contiguous or zigzag layout all P
- *   steps run inside one kernel launch (cp_ring_forward_fused; the workspace
- *   is then unused); otherwise (fp32 inputs, striped layout) one launch per
- *   step covers all ranks and merges into the accumulator
- *   (cp_ring_forward_steps).
+ *   Execution: with bf16 inputs (any layout) all P steps run inside one
+ *   kernel launch (cp_ring_forward_fused; the workspace is then unused);
+ *   with fp32 inputs one launch per step covers all ranks and merges into
+ *   the accumulator (cp_ring_forward_steps).
  *   out [S,H,D] out_dt, lse [H,S] fp32.  workspace: device memory of
  *   cp_ring_workspace_size() bytes (NULL allowed when that is 0).
  *   The result equals cp_attn_block over the whole sequence up to rounding.
@@ -174,8 +173,10 @@ int cp_ring_forward_steps(const void* q, const void* k, const void* v, cp_dtype 
  *   carries the running max, sum and unnormalised output from one step to
  *   the next on chip and writes (out, lse) once.  The result equals
  *   cp_ring_forward_steps' up to rounding (the same terms merged in another
- *   grouping).  bf16 inputs (D = 128) in the contiguous or zigzag layout
- *   (other cases return CP_ERR_DTYPE / CP_ERR_ARG); any S, 1 <= P <=
+ *   grouping).  Striped: the tile of stripe r walks stripes r, r-1, ...,
+ *   each a causal prefix in stripe indices (key i visible to query i' when
+ *   i + (stripe > r) <= i').  bf16 inputs (D = 128), any layout (fp32
+ *   inputs return CP_ERR_DTYPE); any S the layout allows, 1 <= P <=
  *   CP_MAX_RANKS; no workspace.  Arguments otherwise as cp_ring_forward,
  *   which takes this path for those inputs.
  */
@@ -195,13 +196,13 @@ int cp_ring_forward_fused(const void* q, const void* k, const void* v, cp_dtype 
  *
  *   Same arguments, layout and results as cp_ring_forward, minus the
  *   workspace.  When cp_ring_forward runs the ring step by step (fp32
- *   inputs, or the striped layout) with out_dt = CP_BF16, the fp32
+ *   inputs) with out_dt = CP_BF16, the fp32
  *   accumulator lives in a 64 MiB array inside the library (static device
  *   memory every GPU that loads the library holds until process exit), so
  *   S*H*D must be <= 16,777,216 (S = 16384 at H = 8, D = 128); larger sizes
  *   return CP_ERR_SHAPE with a message.  With out_dt = CP_F32, or for a ring
- *   cp_ring_forward runs in one launch (bf16 inputs, contiguous or zigzag),
- *   no scratch is used at all.  The call allocates nothing.
+ *   cp_ring_forward runs in one launch (bf16 inputs), no scratch is used at
+ *   all.  The call allocates nothing.
  *   The first call on a device looks up the array's device address (a
  *   one-time host set-up per device, done with that device current); make
  *   that first call before any stream capture.
@@ -402,8 +403,8 @@ int cp_ulysses_stage(const void* q, const void* k, const void* v, cp_dtype in_dt
  *   in place when Pu is a multiple of Hkv), then the ring of cp_ring_forward
  *   with Pr ranks and `layout` over each group's whole sequence, then
  *   head_to_seq.  The rings of all Pu groups share each launch: one launch
- *   for the whole ring where cp_ring_forward runs in one (bf16 inputs,
- *   contiguous or zigzag), else one per ring step.
+ *   for the whole ring where cp_ring_forward runs in one (bf16 inputs),
+ *   else one per ring step.
  *   The same arguments as cp_ulysses_forward plus Pr and layout; S % Pu = 0
  *   and the ring's own conditions on (S, Pr, layout).
  *   workspace: cp_usp_workspace_size() bytes.
@@ -418,7 +419,7 @@ int cp_usp_forward(const void* q, const void* k, const void* v, cp_dtype in_dt, 
  * cp_usp_stage - one stage of cp_usp_forward (same arguments plus `stage`):
  * 0 = seq_to_head of q, k, v, 1 .. Pr = ring step stage-1 (one launch over
  * all Pu groups), Pr + 1 = head_to_seq of the output.  Where the ring runs
- * in one launch (bf16 inputs, contiguous or zigzag), stage 1 is the whole
+ * in one launch (bf16 inputs), stage 1 is the whole
  * ring and stages 2 .. Pr launch nothing.  Stages 0 .. Pr + 1 in order on
  * one stream are cp_usp_forward, bit for bit.  Other stages: CP_ERR_ARG.
  */

@@ -250,8 +250,8 @@ def test_header_constants_match_the_binding(cp):
 
 
 def test_fused_ring_validation_without_gpu(cp):
-    """The one-launch ring takes bf16 inputs in the contiguous or zigzag
-    layout only; it rejects the rest before any device work."""
+    """The one-launch ring takes bf16 inputs (any layout, with the layout's
+    own conditions); it rejects the rest before any device work."""
     L = cp.lib()
     F32, BF16 = cp.CP_F32, cp.CP_BF16
     ptr = ctypes.c_void_p(256)
@@ -259,7 +259,8 @@ def test_fused_ring_validation_without_gpu(cp):
                                         ptr, None)
     assert L.cp_ring_forward_fused(*args(F32, 16, cp.CP_ZIGZAG, 2)) == -3
     assert "bf16" in cp.cp_last_error()
-    assert L.cp_ring_forward_fused(*args(BF16, 128, cp.CP_STRIPED, 2)) == -1
+    assert L.cp_ring_forward_fused(*args(BF16, 128, cp.CP_STRIPED, 3)) == -2  # S % P != 0
+    assert L.cp_ring_forward_fused(*args(BF16, 128, 7, 2)) == -1  # no such layout
     assert L.cp_ring_forward_fused(*args(BF16, 128, cp.CP_ZIGZAG, 17)) == -1
     assert L.cp_ring_forward_fused(*args(BF16, 64, cp.CP_ZIGZAG, 2)) == -2
     bad = ctypes.c_void_p(258)

@@ -66,7 +66,7 @@ def qkv4k():
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous", "striped"])
 def test_ring_4k_all_rows(cp, qkv4k, layout, out_dtype):
     """S=4096, H=32, D=128, bf16, P=4: every row and head, through
     cp_ring_forward (all steps in one launch for bf16) and through the
@@ -94,7 +94,13 @@ def test_ring_4k_all_rows(cp, qkv4k, layout, out_dtype):
                                               (1000, 8, 4, 3, "contiguous"),
                                               (300, 4, 2, 8, "zigzag"),     # 19-row chunks
                                               (5, 2, 1, 4, "zigzag"),       # empty chunks
-                                              (129, 2, 2, 2, "contiguous")])
+                                              (129, 2, 2, 2, "contiguous"),
+                                              (2048, 4, 2, 4, "striped"),
+                                              (1024, 8, 2, 8, "striped"),
+                                              (4096, 2, 1, 16, "striped"),
+                                              (1000, 4, 4, 8, "striped"),   # 125-row stripes
+                                              (96, 2, 2, 3, "striped"),     # 32-row stripes
+                                              (7, 2, 1, 7, "striped")])     # 1-row stripes
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_ring_fused_against_oracle(cp, S, H, Hkv, P, layout, out_dtype):
     """cp_ring_forward_fused (every step of the ring inside one launch, the
@@ -233,7 +239,7 @@ def test_ring_32k_zigzag_sampled(cp):
     _sampled_check(cp, 32768, 32, 32, 8, "zigzag")
 
 
-@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous", "striped"])
 def test_ring_128k_sampled(cp, layout):
     _sampled_check(cp, 131072, 32, 32, 8, layout)
 
