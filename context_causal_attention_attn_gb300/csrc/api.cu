@@ -682,6 +682,7 @@ struct BwdTask {
   std::vector<BwdItem> items;
   std::vector<int> chunk;
   int64_t ring_C = 0, ring_S = 0;  // chunk geometry of chunk-list items
+  bool striped = false;            // chunk-list items name stripes
 };
 
 struct BwdArgs {
@@ -724,6 +725,7 @@ int run_bwd_task(const BwdArgs& a, const BwdTask& t, const CUtensorMap maps[4], 
   p.ld = a.ld;
   p.ring_C = t.ring_C;
   p.ring_S = t.ring_S;
+  p.ring_striped = t.striped ? 1 : 0;
   p.q_rows = a.q_rows;
   p.k_rows = a.k_rows;
   if (t.dkdv) {
@@ -887,6 +889,27 @@ std::vector<BwdTask> ring_bwd_tasks(int64_t S, int P, cp_layout layout) {
 // Each stationary tile keeps its gradient in TMEM across all steps and
 // writes it once.
 std::vector<BwdTask> ring_bwd_fused_tasks(int64_t S, int P, cp_layout layout) {
+  if (layout == CP_STRIPED) {
+    // every (key stripe, query stripe) pair has visible keys: the dK/dV item
+    // of stripe c streams stripes c, c+1, ... (its holders at steps 0, 1,
+    // ...), the dQ item of stripe r streams stripes r, r-1, ...
+    const int64_t C = S / P;
+    BwdTask tk{true, {}, {}, C, S, true}, tq{false, {}, {}, C, S, true};
+    for (int c = 0; c < P; ++c) {
+      BwdItem kt{}, qt{};
+      kt.stat = BwdSeg{0, 0, static_cast<int32_t>(C), c};
+      qt.stat = BwdSeg{0, 0, static_cast<int32_t>(C), c};
+      for (int t = 0; t < P; ++t) {
+        kt.chunk[kt.nchunk++] = static_cast<uint8_t>((c + t) % P);
+        qt.chunk[qt.nchunk++] = static_cast<uint8_t>(((c - t) % P + P) % P);
+      }
+      tk.items.push_back(kt);
+      tk.chunk.push_back(c);
+      tq.items.push_back(qt);
+      tq.chunk.push_back(c);
+    }
+    return {tk, tq};
+  }
   const int64_t nchunks = layout == CP_ZIGZAG ? 2 * P : P;
   const int64_t C = (S + nchunks - 1) / nchunks;
   auto rows = [&](int c) -> int32_t {
@@ -944,7 +967,7 @@ std::vector<BwdTask> ring_bwd_fused_tasks(int64_t S, int P, cp_layout layout) {
     std::vector<size_t> o(t.items.size());
     for (size_t i = 0; i < o.size(); ++i) o[i] = i;
     std::stable_sort(o.begin(), o.end(), [&](size_t a, size_t b) { return w[a] > w[b]; });
-    BwdTask s{t.dkdv, {}, {}, t.ring_C, t.ring_S};
+    BwdTask s{t.dkdv, {}, {}, t.ring_C, t.ring_S, t.striped};
     for (size_t i : o) {
       s.items.push_back(t.items[i]);
       s.chunk.push_back(t.chunk[i]);
@@ -984,10 +1007,10 @@ bool ring_runs_fused(cp_dtype in_dt, cp_layout layout) {
          (layout == CP_CONTIGUOUS || layout == CP_ZIGZAG || layout == CP_STRIPED);
 }
 
-// Whether cp_ring_backward runs in two launches over all steps: bf16 inputs
-// in the contiguous or zigzag layout.
+// Whether cp_ring_backward runs in two launches over all steps: bf16 inputs,
+// any layout.
 bool ring_bwd_runs_fused(cp_dtype in_dt, cp_layout layout) {
-  return in_dt == CP_BF16 && (layout == CP_CONTIGUOUS || layout == CP_ZIGZAG);
+  return ring_runs_fused(in_dt, layout);
 }
 }  // namespace cpattn
 
@@ -1842,8 +1865,7 @@ static int ring_backward_launch(const void* q, const void* k, const void* v, con
   if ((rc = check_ring(in_dt, S, H, Hkv, D, P, layout, grad_dt)) != CP_OK) return rc;
   if (fused && !ring_bwd_runs_fused(in_dt, layout))
     return fail(in_dt != CP_BF16 ? CP_ERR_DTYPE : CP_ERR_ARG,
-                "the two-launch ring backward needs bf16 inputs and the contiguous or zigzag "
-                "layout");
+                "the two-launch ring backward needs bf16 inputs");
   const int nl = fused ? 2 : 2 * P;
   if (launch < -1 || launch >= nl)
     return fail(CP_ERR_ARG, "launch=%d outside [-1,%d)", launch, nl);

@@ -115,9 +115,20 @@ __device__ __forceinline__ int bw_tiles(int len) { return (len + bw::BN - 1) / b
 __device__ __forceinline__ int bw_nstr(const BwdItem& it) {
   return it.nchunk > 0 ? it.nchunk : it.nstr;
 }
+template <bool kDKDV>
 __device__ __forceinline__ void bw_str(const BwdItem& it, const BwdParams& p, int s,
                                        int64_t& row, int64_t& pos, int& len, int& stripe) {
-  if (it.nchunk > 0) {
+  if (it.nchunk > 0 && p.ring_striped) {
+    // stripe c in stripe indices.  Key i of stripe a sees query i' of stripe
+    // b when i + (a > b) <= i': streamed keys (dQ) sit one position later
+    // when their stripe follows the queries'; streamed queries (dK/dV) one
+    // position earlier when the keys' stripe follows theirs.
+    const int c = it.chunk[s];
+    row = 0;
+    pos = kDKDV ? (it.stat.stripe > c ? -1 : 0) : (c > it.stat.stripe ? 1 : 0);
+    len = static_cast<int>(p.ring_C);
+    stripe = c;
+  } else if (it.nchunk > 0) {
     const int64_t c0 = static_cast<int64_t>(it.chunk[s]) * p.ring_C;
     row = c0;
     pos = c0;
@@ -168,7 +179,7 @@ __device__ __forceinline__ int bw_count(const BwdItem& it, const BwdParams& p, i
   for (int s = 0; s < ns; ++s) {
     int64_t row, pos;
     int len, stripe, t0, t1;
-    bw_str(it, p, s, row, pos, len, stripe);
+    bw_str<kDKDV>(it, p, s, row, pos, len, stripe);
     bw_vis<kDKDV>(pos, len, lim_pos, causal, t0, t1);
     n += t1 - t0;
   }
@@ -188,7 +199,7 @@ struct BwCursor {
     for (; s < ns; ++s) {
       int64_t row, pos;
       int len, stripe, t0;
-      bw_str(it, p, s, row, pos, len, stripe);
+      bw_str<kDKDV>(it, p, s, row, pos, len, stripe);
       bw_vis<kDKDV>(pos, len, lim, causal, t0, tend);
       if (t0 < tend) {
         t = t0;
@@ -224,7 +235,7 @@ struct BwCursor {
   __device__ __forceinline__ void tile(const BwdItem& it, const BwdParams& p, int64_t& row,
                                        int64_t& pos, int& n, int& stripe) const {
     int len;
-    bw_str(it, p, s, row, pos, len, stripe);
+    bw_str<kDKDV>(it, p, s, row, pos, len, stripe);
     row += static_cast<int64_t>(t) * bw::BN;
     pos += static_cast<int64_t>(t) * bw::BN;
     n = min(bw::BN, len - t * bw::BN);

@@ -190,7 +190,9 @@ struct BwdItem {
   // A whole ring in one launch: when nchunk > 0 the streamed segments are
   // the sequence chunks chunk[0..nchunk) in the order the ring's steps reach
   // them (chunk c = rows [c C, min(S, (c+1) C)) with C = BwdParams::ring_C,
-  // S = BwdParams::ring_S), and str / nstr are unused.
+  // S = BwdParams::ring_S), and str / nstr are unused.  With
+  // BwdParams::ring_striped they are stripes (C = S / P rows of stripe c),
+  // key i of stripe a visible to query i' of stripe b when i + (a > b) <= i'.
   int32_t nchunk;
   uint8_t chunk[kMaxRingChunks];
 };
@@ -213,6 +215,7 @@ struct BwdParams {
   BwdItem items[kMaxItems];
   int64_t ring_C, ring_S;  // chunk rows and sequence length of chunk-list items
   int64_t q_rows, k_rows;  // rows of the q / dout / dq and k / v / dk / dv tensors (bounds)
+  int ring_striped;        // chunk-list items name stripes (see BwdItem::chunk)
 };
 
 }  // namespace cpattn

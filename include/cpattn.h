@@ -468,9 +468,9 @@ int cp_attn_block_backward(const void* q, const void* k, const void* v, const vo
  * same ring schedule: at step t virtual rank r evaluates the forward's
  * (query chunk, held KV chunk) pairs; dQ of its chunks accumulates in place,
  * dK / dV accumulate on the held chunk (in the ring they travel with it back
- * to their owner).  For bf16 inputs in the contiguous or zigzag layout one
- * dK/dV launch and one dQ launch cover every step (cp_ring_backward_fused_step),
- * otherwise one of each per step covers all ranks (cp_ring_backward_step);
+ * to their owner).  For bf16 inputs (any layout) one dK/dV launch and one
+ * dQ launch cover every step (cp_ring_backward_fused_step), for fp32 inputs
+ * one of each per step covers all ranks (cp_ring_backward_step);
  * the blocks use the whole-row lse, so the result equals the gradients of
  * monolithic causal attention up to rounding.
  *
@@ -490,12 +490,12 @@ int64_t cp_ring_backward_workspace_size(int64_t S, int H, int Hkv, int D, cp_dty
  * launch = 2t: the dK/dV kernel of ring step t, accumulating into the fp32
  * gradient buffers; launch = 2t + 1: the dQ kernel of step t (0 <= t < P).
  * Running launch -1, 0, 1, ..., 2P-1 in order on one stream is the ring
- * backward step by step -- what cp_ring_backward runs for fp32 inputs and
- * the striped layout.  Arguments as cp_ring_backward.
+ * backward step by step -- what cp_ring_backward runs for fp32 inputs.
+ * Arguments as cp_ring_backward.
  *
  * cp_ring_backward_fused_step - one launch of the two-launch schedule that
- * cp_ring_backward runs for bf16 inputs in the contiguous or zigzag layout
- * (other inputs return CP_ERR_DTYPE / CP_ERR_ARG).  launch = -1: delta;
+ * cp_ring_backward runs for bf16 inputs (fp32 inputs return CP_ERR_DTYPE).
+ * launch = -1: delta;
  * launch = 0: the dK/dV kernel over every ring step -- each KV tile stays
  * put while the query chunks that see it stream past in the order the
  * ring's steps bring them to its holder, its dK / dV held in TMEM and

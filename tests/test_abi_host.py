@@ -269,7 +269,7 @@ def test_fused_ring_validation_without_gpu(cp):
 
 
 def test_fused_ring_backward_validation_without_gpu(cp):
-    """The two-launch ring backward takes bf16 contiguous / zigzag rings and
+    """The two-launch ring backward takes bf16 rings (any layout) and
     launches -1, 0, 1; anything else is rejected before any device work."""
     L = cp.lib()
     F32, BF16 = cp.CP_F32, cp.CP_BF16
@@ -279,7 +279,9 @@ def test_fused_ring_backward_validation_without_gpu(cp):
         return L.cp_ring_backward_fused_step(p, p, p, p, p, p, in_dt, 256, 4, 4, D, 2, layout,
                                              launch, p, p, p, BF16, p, None)
     assert call(F32, 16, cp.CP_ZIGZAG, 0) == -3
-    assert call(BF16, 128, cp.CP_STRIPED, 0) == -1
+    assert call(BF16, 128, 9, 0) == -1  # no such layout
+    assert call(BF16, 128, cp.CP_STRIPED, 2) == -1
+    assert "launch" in cp.cp_last_error()
     assert call(BF16, 128, cp.CP_ZIGZAG, 2) == -1
     assert "launch" in cp.cp_last_error()
     assert call(BF16, 128, cp.CP_ZIGZAG, -2) == -1

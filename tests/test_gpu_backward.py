@@ -262,7 +262,7 @@ def test_ring_backward_matches_block_sum(cp):
         assert diff <= 1e-4 * want.abs().max().item(), f"{name}: ring vs block sum {diff:.3e}"
 
 
-@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous", "striped"])
 def test_ring_backward_steps_equal_whole(cp, layout):
     """cp_ring_backward (bf16: two launches over every step) is
     cp_ring_backward_fused_step over launches -1, 0, 1, bit for bit; the
@@ -290,12 +290,15 @@ def test_ring_backward_steps_equal_whole(cp, layout):
 @pytest.mark.parametrize("layout,S,P,Hkv", [("zigzag", 4096, 8, 2), ("zigzag", 4096, 16, 4),
                                             ("contiguous", 4096, 8, 4), ("zigzag", 1000, 3, 2),
                                             ("contiguous", 1500, 4, 1), ("zigzag", 300, 8, 4),
-                                            ("zigzag", 2048, 1, 4)])
+                                            ("zigzag", 2048, 1, 4), ("striped", 4096, 8, 2),
+                                            ("striped", 1200, 6, 4), ("striped", 2048, 16, 1),
+                                            ("striped", 96, 3, 2)])
 def test_ring_backward_fused_against_oracle(cp, layout, S, P, Hkv):
     """The two-launch ring backward (every step inside one dK/dV and one dQ
     launch) against the oracle's monolithic gradients: degrees 1..16, GQA
     4:1 .. 4:4, chunks that are not multiples of the 128-row tile, a short
-    last chunk; guard bands around the gradients."""
+    last chunk, striped rings (200- and 32-row stripes among them); guard
+    bands around the gradients."""
     q, k, v, do, ob, l32 = forward_inputs(S, 4, Hkv, seed=S + P + Hkv)
     (dq, dq_ok), (dk, dk_ok), (dv, dv_ok) = (guarded(t.shape, torch.float32) for t in (q, k, v))
     cp.cp_ring_backward(*dev(q, k, v, ob, do, l32), P, layout, dq=dq, dk=dk, dv=dv)
