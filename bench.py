@@ -4,11 +4,10 @@
     python bench.py --impl reference ...      (the fp64 CPU oracle, timed)
 
 One step = one full ring forward over the sequence (all P virtual-rank steps)
-through cp_ring_forward, on inputs already resident in HBM: for bf16 rings in
-the contiguous or zigzag layout all steps run in one launch (each query tile
-walks its rank's held KV chunks in step order and merges on chip); the
-_steps workloads and the striped layout run one launch per step with the LSE
-merge in the attention epilogue.  Prints ONE JSON line on rank 0.
+through cp_ring_forward, on inputs already resident in HBM: for bf16 rings
+all steps run in one launch (each query tile walks its rank's held KV chunks
+in step order and merges on chip); the _steps workloads run one launch per
+step with the LSE merge in the attention epilogue.  Prints ONE JSON line on rank 0.
 
 Workloads (synthetic, seeded N(0,1) inputs, the handbook's make_qkv recipe):
   ring128k_zigzag (default)  S=131072 H=32 D=128 bf16, P=8 zigzag
@@ -774,8 +773,8 @@ def run_bwd(args, wl, rank, world, local):
     # ring where it runs fused, else one per step)
     fwd_launches = [("fwd", -1)] if cp.ring_runs_fused(q, layout) else [
         ("fwd", t) for t in range(P)]
-    # the backward: cp_ring_backward's schedule (for bf16 contiguous / zigzag
-    # one dK/dV and one dQ launch over every step, else one of each per step)
+    # the backward: cp_ring_backward's schedule (for bf16 inputs one dK/dV and
+    # one dQ launch over every step, else one of each per step)
     fused_bwd = cp.ring_backward_runs_fused(q, layout)
     bstep = cp.cp_ring_backward_fused_step if fused_bwd else cp.cp_ring_backward_step
     nbl = 2 if fused_bwd else 2 * P

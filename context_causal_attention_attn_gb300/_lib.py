@@ -233,8 +233,8 @@ def ring_runs_fused(q, layout):
 
 def ring_backward_runs_fused(q, layout):
     """Whether cp_ring_backward runs in two launches over all steps (bf16
-    inputs, contiguous or zigzag)."""
-    return q.dtype == torch.bfloat16 and layout in ("contiguous", "zigzag")
+    inputs, any layout)."""
+    return q.dtype == torch.bfloat16 and layout in ("contiguous", "zigzag", "striped")
 
 
 def cp_ring_forward(q, k, v, P, layout="zigzag", out=None, out_dtype=None, lse=None,
@@ -712,7 +712,7 @@ def cp_ring_backward_step(q, k, v, out, dout, lse, P, layout, launch, dq, dk, dv
 
 def cp_ring_backward_fused_step(q, k, v, out, dout, lse, P, layout, launch, dq, dk, dv,
                                 workspace, stream=None):
-    """One launch of the two-launch ring backward (bf16, contiguous or zigzag):
+    """One launch of the two-launch ring backward (bf16 inputs):
     -1 delta, 0 dK/dV over every step, 1 dQ over every step."""
     S, H, D = q.shape
     Hkv = k.shape[1]

@@ -459,8 +459,8 @@ int head_major_lead(const std::vector<WorkItem>& items, int64_t C, int64_t S, bo
   return static_cast<int>(lead);
 }
 
-// The ring in one launch (bf16 inputs, contiguous or zigzag layout): one
-// work item per (virtual rank r, own query chunk qc), whose key segments are
+// The ring in one launch (bf16 inputs): one work item per (virtual rank r,
+// own query chunk qc; in the striped layout its stripe), whose key segments are
 // the chunks rank r holds at steps t = 0, 1, ..., P-1 (src = (r - t) mod P,
 // ascending within a step) that are not later than qc -- exactly the blocks
 // the per-step ring evaluates for those rows, in the same order.  Each query
@@ -880,7 +880,7 @@ std::vector<BwdTask> ring_bwd_tasks(int64_t S, int P, cp_layout layout) {
   return tasks;
 }
 
-// The ring's backward in two launches (bf16, contiguous or zigzag): the dK/dV
+// The ring's backward in two launches (bf16 inputs): the dK/dV
 // kernel runs one item per KV chunk, streaming the query chunks that see it
 // in the order the ring's steps bring them (at step t the chunk sits with
 // rank owner + t, whose own query chunks not earlier than it are evaluated);
