@@ -115,13 +115,14 @@ __device__ __forceinline__ int bw_tiles(int len) { return (len + bw::BN - 1) / b
 __device__ __forceinline__ int bw_nstr(const BwdItem& it) {
   return it.nchunk > 0 ? it.nchunk : it.nstr;
 }
-template <bool kDKDV>
+template <bool kDKDV, bool kStriped>
 __device__ __forceinline__ void bw_str(const BwdItem& it, const BwdParams& p, int s,
                                        int64_t& row, int64_t& pos, int& len, int& stripe) {
-  if (it.nchunk > 0 && p.ring_striped) {
-    // stripe c in stripe indices.  Key i of stripe a sees query i' of stripe
-    // b when i + (a > b) <= i': streamed keys (dQ) sit one position later
-    // when their stripe follows the queries'; streamed queries (dK/dV) one
+  if (kStriped && it.nchunk > 0 && p.ring_striped) {
+    // stripe c in stripe indices (only kernels with strided rows see
+    // these).  Key i of stripe a sees query i' of stripe b when
+    // i + (a > b) <= i': streamed keys (dQ) sit one position later when
+    // their stripe follows the queries'; streamed queries (dK/dV) one
     // position earlier when the keys' stripe follows theirs.
     const int c = it.chunk[s];
     row = 0;
@@ -171,7 +172,7 @@ __device__ __forceinline__ void bw_vis(int64_t pos, int len, int64_t lim_pos, bo
 
 // Streamed tiles of an item per head (the dK/dV kernel runs them once per
 // query head of its group).
-template <bool kDKDV>
+template <bool kDKDV, bool kStriped>
 __device__ __forceinline__ int bw_count(const BwdItem& it, const BwdParams& p, int64_t lim_pos,
                                         bool causal) {
   int n = 0;
@@ -179,7 +180,7 @@ __device__ __forceinline__ int bw_count(const BwdItem& it, const BwdParams& p, i
   for (int s = 0; s < ns; ++s) {
     int64_t row, pos;
     int len, stripe, t0, t1;
-    bw_str<kDKDV>(it, p, s, row, pos, len, stripe);
+    bw_str<kDKDV, kStriped>(it, p, s, row, pos, len, stripe);
     bw_vis<kDKDV>(pos, len, lim_pos, causal, t0, t1);
     n += t1 - t0;
   }
@@ -189,7 +190,7 @@ __device__ __forceinline__ int bw_count(const BwdItem& it, const BwdParams& p, i
 // Walks the streamed tiles of an item in order -- segment by segment, and
 // for the dK/dV kernel head by head of the query group -- keeping only its
 // position (a tile's rows are re-derived from the item when asked for).
-template <bool kDKDV>
+template <bool kDKDV, bool kStriped>
 struct BwCursor {
   int s, t, tend;  // segment, tile within it, end of its used tiles
   int k, g;        // tile within the head, query head within the group
@@ -199,7 +200,7 @@ struct BwCursor {
     for (; s < ns; ++s) {
       int64_t row, pos;
       int len, stripe, t0;
-      bw_str<kDKDV>(it, p, s, row, pos, len, stripe);
+      bw_str<kDKDV, kStriped>(it, p, s, row, pos, len, stripe);
       bw_vis<kDKDV>(pos, len, lim, causal, t0, tend);
       if (t0 < tend) {
         t = t0;
@@ -235,7 +236,7 @@ struct BwCursor {
   __device__ __forceinline__ void tile(const BwdItem& it, const BwdParams& p, int64_t& row,
                                        int64_t& pos, int& n, int& stripe) const {
     int len;
-    bw_str<kDKDV>(it, p, s, row, pos, len, stripe);
+    bw_str<kDKDV, kStriped>(it, p, s, row, pos, len, stripe);
     row += static_cast<int64_t>(t) * bw::BN;
     pos += static_cast<int64_t>(t) * bw::BN;
     n = min(bw::BN, len - t * bw::BN);
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   const int nstat = min(bw::BM, it.stat.len - stile * bw::BM);
   // visibility limit: last query position (dQ) / first key position (dK/dV)
   const int64_t lim = kDKDV ? spos0 : spos0 + nstat - 1;
-  const int nper = bw_count<kDKDV>(it, p, lim, causal);
+  const int nper = bw_count<kDKDV, kStriped>(it, p, lim, causal);
   const int nstr = kDKDV ? nper * grp : nper;
   const int kvh = kDKDV ? shead : shead / grp;
   const int64_t stride = kStriped ? p.stride : 1;
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   auto slot_of = [](int j, int w) { return w == 0 ? j % NA : NA + j % NB; };
   auto use_of = [](int j, int w) { return w == 0 ? j / NA : j / NB; };
   // the cursor's tile -> (row, pos, rows, stripe, query head), then advance
-  auto str_tile = [&](BwCursor<kDKDV>& c, int64_t& row, int64_t& pos, int& n, int& stripe,
+  auto str_tile = [&](BwCursor<kDKDV, kStriped>& c, int64_t& row, int64_t& pos, int& n, int& stripe,
                       int& qh) {
     c.tile(it, p, row, pos, n, stripe);
     qh = kDKDV ? shead * grp + c.g : shead;
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
           load(sStat + w * bw::TILE_BYTES + hh * bw::BOX_BYTES, w == 0 ? st0 : st1,
                bar(bw::BAR_STAT), hh * 64, sh, it.stat.stripe, srow0, pol_stat);
       int issued = 0;  // tiles whose loads were issued
-      BwCursor<kDKDV> pc;
+      BwCursor<kDKDV, kStriped> pc;
       pc.init(it, p, lim, causal);
       for (int j = 0; j < nstr; ++j) {
         int64_t row, pos;
@@ -563,7 +564,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const int ccol = etid & (bw::BN - 1);
     const bool is_l = etid < bw::BN;
     // cursors of the tile loop and of the column loads (one tile ahead)
-    BwCursor<kDKDV> cc, lc;
+    BwCursor<kDKDV, kStriped> cc, lc;
     cc.init(it, p, lim, causal);
     lc = cc;
     // the next tile's column value; called for tiles 0, 1, ... in order

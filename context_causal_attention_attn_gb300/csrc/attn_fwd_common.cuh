@@ -1,6 +1,6 @@
-// Pieces shared by the forward attention kernels on the tensor cores
-// (attn_tc.cu, attn_tc1.cu): tile sizes, the walk over an item's KV tiles,
-// and the timeout record.
+// Pieces of the forward attention kernel on the tensor cores (attn_tc.cu):
+// tile sizes, the walk over an item's KV tiles, the task decode's search and
+// the timeout record.
 #pragma once
 
 #include <stdint.h>
@@ -25,9 +25,12 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 __device__ __forceinline__ int item_nseg(const WorkItem& it) {
   return it.nchunk > 0 ? it.nchunk : it.nseg;
 }
+// kStriped: the kernel instance with strided rows (the only one that sees
+// striped chunk lists, whose check the plain instance compiles away).
+template <bool kStriped>
 __device__ __forceinline__ void item_seg(const WorkItem& it, const AttnParams& p, int s,
                                          int64_t& mem_row, int64_t& pos, int& len, int& stripe) {
-  if (it.nchunk > 0 && p.ring_striped) {
+  if (kStriped && it.nchunk > 0 && p.ring_striped) {
     // stripe c in stripe indices; its keys trail the queries' by one
     // position when c comes after the query stripe
     const int c = it.chunk[s];
@@ -65,6 +68,7 @@ __device__ __forceinline__ int seg_visible_tiles(int64_t pos, int len, int64_t q
 // prefix of all tiles; for chunk-list items the diagonal chunk may come
 // before earlier ones.)  Only the position in the walk is kept (three
 // registers); a tile's keys are re-derived from the item when asked for.
+template <bool kStriped>
 struct TileCursor {
   int s, t, tv;  // segment, tile within it, visible tiles of the segment
   __device__ __forceinline__ void seek(const WorkItem& it, const AttnParams& p, int64_t qp_last,
@@ -73,7 +77,7 @@ struct TileCursor {
     for (; s < n; ++s) {
       int64_t mem_row, pos;
       int len, stripe;
-      item_seg(it, p, s, mem_row, pos, len, stripe);
+      item_seg<kStriped>(it, p, s, mem_row, pos, len, stripe);
       tv = seg_visible_tiles(pos, len, qp_last, causal);
       if (tv > 0) return;
     }
@@ -98,7 +102,7 @@ struct TileCursor {
   __device__ __forceinline__ void keys(const WorkItem& it, const AttnParams& p, int64_t& kmem,
                                        int64_t& kpos, int& nk, int& stripe) const {
     int len;
-    item_seg(it, p, s, kmem, kpos, len, stripe);
+    item_seg<kStriped>(it, p, s, kmem, kpos, len, stripe);
     kmem += static_cast<int64_t>(t) * tc::BN;
     kpos += static_cast<int64_t>(t) * tc::BN;
     nk = min(tc::BN, len - t * tc::BN);
@@ -106,9 +110,10 @@ struct TileCursor {
 };
 
 // Number of KV tiles a query tile whose last row sits at qp_last evaluates.
+template <bool kStriped>
 __device__ __forceinline__ int visible_tiles(const WorkItem& it, const AttnParams& p,
                                              int64_t qp_last, bool causal) {
-  if (it.nchunk > 0 && causal && !p.ring_striped) {
+  if (it.nchunk > 0 && causal && !(kStriped && p.ring_striped)) {
     // every chunk but the query chunk lies before it
     const int64_t pos = static_cast<int64_t>(it.q_chunk) * p.ring_C;
     const int len = static_cast<int>(min(p.ring_S - pos, p.ring_C));
@@ -119,7 +124,7 @@ __device__ __forceinline__ int visible_tiles(const WorkItem& it, const AttnParam
   for (int s = 0; s < ns; ++s) {
     int64_t mem_row, pos;
     int len, stripe;
-    item_seg(it, p, s, mem_row, pos, len, stripe);
+    item_seg<kStriped>(it, p, s, mem_row, pos, len, stripe);
     n += seg_visible_tiles(pos, len, qp_last, causal);
   }
   return n;

@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
   const int64_t k_boff = static_cast<int64_t>(b) * it.b_k_rows;
   const int nrows_a = min(tc::BM, it.sq - row0);
   const int nrows_b = NT == 2 ? max(0, min(tc::BM, it.sq - row0 - tc::BM)) : 0;
-  const int n_a = visible_tiles(it, p, q_pos0 + nrows_a - 1, causal);
-  const int n_b = nrows_b > 0 ? visible_tiles(it, p, q_pos0 + tc::BM + nrows_b - 1, causal) : 0;
+  const int n_a = visible_tiles<kStriped>(it, p, q_pos0 + nrows_a - 1, causal);
+  const int n_b =
+      nrows_b > 0 ? visible_tiles<kStriped>(it, p, q_pos0 + tc::BM + nrows_b - 1, causal) : 0;
   const int nkv = max(n_a, n_b);
   // Bounds-checked build: the tile's q rows, out / acc rows and lse columns
   // lie inside their tensors (out has the rows of q); a tile that fails is
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
   const bool producer = warp == C::WARP_LOAD && lane == 0;
   uint64_t pol_q = 0, pol_kv = 0;
   int issued = 0;  // producer: K/V copies issued
-  TileCursor pcur;  // producer: the next tile to load
+  TileCursor<kStriped> pcur;  // producer: the next tile to load
   // K_j and V_j into the next stages (n = 2 j + w), each once its stage is
   // released; false when a wait expired.  Called for j = 0, 1, ... in order.
   auto issue_kv = [&](int j) -> bool {
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         }
         if (row < nrows) cp_async4(sbase + C::OFF_LSE + row * 4, lse_addr());
       };
-      TileCursor cur;
+      TileCursor<kStriped> cur;
       cur.init(it, p, qp_first + nrows - 1, causal);
       for (int j = 0; j < nx; ++j) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(bar(C::BAR_S_FULL + x), j & 1,
