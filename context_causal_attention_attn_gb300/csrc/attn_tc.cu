@@ -483,13 +483,12 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         for (int c = 8; c < tc::BN; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
         const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // the exponent base moves only when the row max grows by more than
+        // the threshold; the rescale factor is derived after the
+        // exponentials, so that only m_prev stays live across them
         const float m_new = fmaxf(m_used, mx * sl2);
-        float alpha = 1.f;
-        const bool grow = m_new > m_used + tc::RESCALE_THRESHOLD;
-        if (grow) {
-          alpha = ex2_approx(m_used - m_new);
-          m_used = m_new;
-        }
+        const float m_prev = m_used;
+        if (m_new > m_used + tc::RESCALE_THRESHOLD) m_used = m_new;
         const float base = m_used == -CUDART_INF_F ? 0.f : m_used;
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nbx2 = f2_pack(-base, -base);
         uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
@@ -516,6 +515,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         f2_unpack(rs2[0], rs4[0], rs4[1]);
         f2_unpack(rs2[1], rs4[2], rs4[3]);
         const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        const bool grow = m_used != m_prev;  // m_used is never NaN
+        const float alpha = grow ? ex2_approx(m_prev - m_used) : 1.f;
         l = fmaf(l, alpha, rs);
         // rescale O_X (no MMA touches it now: PV_X(j-1) completed before S_X(j)
         // was issued, and PV_X(j) waits for the arrival below)
