@@ -239,6 +239,17 @@ def test_ring_32k_zigzag_sampled(cp):
     _sampled_check(cp, 32768, 32, 32, 8, "zigzag")
 
 
+@pytest.mark.parametrize("Hkv,P,layout", [(8, 16, "zigzag"), (32, 8, "contiguous"),
+                                          (4, 4, "striped")])
+def test_ring_32k_more_sampled(cp, Hkv, P, layout):
+    """The one-launch ring at 32K in other shapes of its grid: GQA 32/8 with
+    16 ranks (32 chunks of 1024 rows) and striped with GQA 32/4, whose K/V
+    fits in L2 (the grid runs in the items' order across the heads), and
+    contiguous chunks with 32 KV heads (head by head, shortest tiles last
+    across the heads)."""
+    _sampled_check(cp, 32768, 32, Hkv, P, layout)
+
+
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous", "striped"])
 def test_ring_128k_sampled(cp, layout):
     _sampled_check(cp, 131072, 32, 32, 8, layout)
