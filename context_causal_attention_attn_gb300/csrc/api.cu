@@ -531,7 +531,8 @@ int ring_fused_impl(const void* q, const void* k, const void* v, int64_t S, int 
         }
         w.flags = kFlagCausal | kFlagFinal;
         w.q_chunk = r;
-        for (int t = 0; t < P; ++t) w.chunk[w.nchunk++] = static_cast<uint8_t>(((r - t) % P + P) % P);
+        for (int t = 0; t < P; ++t)
+          w.chunk[w.nchunk++] = static_cast<uint8_t>(((r - t) % P + P) % P);
         L.items.push_back(w);
         work.push_back(C * C * P);  // alike for every rank
         continue;
@@ -916,7 +917,9 @@ std::vector<BwdTask> ring_bwd_fused_tasks(int64_t S, int P, cp_layout layout) {
     return static_cast<int32_t>(std::max<int64_t>(0, std::min<int64_t>(S, (c + 1) * C) - c * C));
   };
   auto seg = [&](int c) { return BwdSeg{c * C, c * C, rows(c), 0}; };
-  auto owner = [&](int c) { return layout == CP_ZIGZAG && c >= P ? static_cast<int>(2 * P - 1 - c) : c; };
+  auto owner = [&](int c) {
+    return layout == CP_ZIGZAG && c >= P ? static_cast<int>(2 * P - 1 - c) : c;
+  };
   BwdTask tk{true, {}, {}, C, S}, tq{false, {}, {}, C, S};
   std::vector<int64_t> wk, wq;  // streamed rows, for the longest-first order
   for (int kc = 0; kc < nchunks; ++kc) {

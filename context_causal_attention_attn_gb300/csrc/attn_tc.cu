@@ -84,9 +84,9 @@ struct Cfg {
   static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // alignment slack
   // Epilogue staging: 128 rows of 512 bytes over the Q buffer and K/V stage 0,
   // both free once the last S MMA is done (K_j always sits in stage 0), so
-  // the merge's accumulator rows are fetched while the last PV runs.  16-byte chunk c of row r sits at chunk c ^ (r & 7): the
-  // row-per-thread and the row-per-warp accesses are both free of bank
-  // conflicts.
+  // the merge's accumulator rows are fetched while the last PV runs.  16-byte
+  // chunk c of row r sits at chunk c ^ (r & 7): the row-per-thread and the
+  // row-per-warp accesses are both free of bank conflicts.
   static constexpr uint32_t STG_BYTES = 128 * 512;
   static_assert(OFF_Q == 0 && OFF_KV + TILE_BYTES == STG_BYTES && STAGES == 2,
                 "staging = Q + K/V stage 0");
@@ -184,8 +184,9 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
     const int64_t lh = static_cast<int64_t>(head) + static_cast<int64_t>(b) * it.b_lse_heads;
     in_bounds = nr > 0 && q_mem0 >= 0 && q_mem0 + nr <= p.q_rows / p.stripe &&
                 it.q_stripe >= 0 && it.q_stripe < p.stripe && kvh >= 0 && kvh < p.Hkv &&
-                o0 >= 0 && o0 + (nr - 1) * os < p.q_rows && lh < static_cast<int64_t>(p.H) * it.batch &&
-                c0 >= 0 && c0 + (nr - 1) * os < p.ld_lse;
+                o0 >= 0 && o0 + (nr - 1) * os < p.q_rows &&
+                lh < static_cast<int64_t>(p.H) * it.batch && c0 >= 0 &&
+                c0 + (nr - 1) * os < p.ld_lse;
     if (threadIdx.x == 0) bounds_ok(in_bounds, dev_err, kSiteFwdTile);
   }
 
@@ -623,7 +624,8 @@ __global__ void __launch_bounds__(tc::Cfg<NT>::THREADS, tc::Cfg<NT>::MIN_BLOCKS)
         fence_proxy_async_smem();  // the staged rows, to the copy engine
         named_bar_sync(1, 128);
         if (row == 0 && *abort_flag == 0) {
-          const int orow0 = static_cast<int>(it.o_row + static_cast<int64_t>(b) * it.b_o_rows + row0);
+          const int orow0 =
+              static_cast<int>(it.o_row + static_cast<int64_t>(b) * it.b_o_rows + row0);
           tma_store_3d(&tm_o, sbase + C::OFF_Q, 0, head, orow0);
           tma_store_3d(&tm_o, sbase + C::OFF_Q + 16384, 64, head, orow0);
           bulk_commit_group();
